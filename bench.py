@@ -1,0 +1,497 @@
+"""Benchmark of the quantized matrix product on GB300.
+
+Headline (one JSON line on stdout): decode qGEMV weight-GB/s on the 2B-class
+MLP projections, INT4 group-64 affine codes: a step is one decode pass through
+L layers, each layer an up-projection (K=2048 -> N=6144) and a
+down-projection (K=6144 -> N=2048) with its own weights and activations.  L
+is chosen so that one step's weights exceed the L2 cache several times, so
+every timed step reads its codes from HBM (no flush needed).  The other
+decode and prefill shapes are measured the same way and reported under
+"per_config".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU with no data exchange (weak scaling); the timed region is bracketed by a
+barrier and the slowest rank's time is used.
+
+--impl reference times the CPU oracle (plain C, FP64, all host cores) on a
+bounded sample of the same workload: the reference arm for this method.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_weight_gb300 import inputs  # noqa: E402
+
+HEADLINE_UP = "decode_int4_up_k2048_n6144"
+HEADLINE_DOWN = "decode_int4_down_k6144_n2048"
+WORKLOAD_NAME = "decode_int4_g64_mlp_up_k2048_n6144+down_k6144_n2048"
+METRIC = "decode qGEMV weight-GB/s (% of HBM peak)"
+NOMINAL_HBM_GBS = 8000.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_int4_decode_mlp.md")
+GEMV_SOURCE = os.path.join(ROOT, "quantized_weight_gb300", "csrc", "gemv.cu")
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def gemv_bytes(M, N, K, bits, group):
+    """Bytes a decode product must move: codes + coefficients + x + y."""
+    codes = N * K * bits // 8
+    coeffs = N * (K // group) * 2 * (2 if bits == 4 else 1)
+    return codes + coeffs + M * K * 4 + M * N * 4
+
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+# ---------------------------------------------------------------- environment
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is under load."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [t.strip() for t in ln.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                util = float(f[4])
+                mhz, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            if util < 5:
+                continue
+            sm.append(mhz)
+            smax.append(mx)
+            for name, v in zip(names, f[6:10]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- device workloads
+
+def device_inputs(name, seed, torch, qmm):
+    w = inputs.WORKLOADS[name]
+    d = inputs.make(w.M, w.N, w.K, w.bits, w.group, seed, w.prefill)
+    dev = "cuda"
+    codes = torch.from_numpy(d["codes"]).to(dev)
+    t = {
+        "packed": qmm.pack(codes, w.bits),
+        "scales": torch.from_numpy(d["scales"].view(np.float16)).to(dev),
+        "biases": None if d["biases"] is None else torch.from_numpy(d["biases"].view(np.float16)).to(dev),
+        "x": torch.from_numpy(d["x"]).to(dev),
+    }
+    if w.prefill:
+        t["x_bf16"] = torch.from_numpy(d["x_bf16"].view(np.int16)).to(dev).view(torch.bfloat16)
+    del codes
+    return w, d, t
+
+
+def replicate(t, copies, torch):
+    """`copies` independent device copies (distinct HBM) of one set of inputs."""
+    out = [t]
+    for _ in range(copies - 1):
+        out.append({k: (None if v is None else v.clone()) for k, v in t.items()})
+    return out
+
+
+def l2_bytes(torch):
+    try:
+        return torch.cuda.get_device_properties(0).L2_cache_size
+    except Exception:
+        return 126 * 1024 * 1024
+
+
+class Chain:
+    """A list of products launched back to back on one stream; captured in a CUDA graph."""
+
+    def __init__(self, calls, torch):
+        self.calls = calls
+        self.torch = torch
+        self.graph = None
+
+    def launch_eager(self):
+        for c in self.calls:
+            c()
+
+    def capture(self, stream):
+        torch = self.torch
+        with torch.cuda.stream(stream):
+            self.launch_eager()          # first run outside capture (loads the kernels)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.launch_eager()
+        self.graph = g
+        return self
+
+    def replay(self):
+        self.graph.replay()
+
+
+def time_graph(chain, reps, warmup, torch, stream):
+    for _ in range(warmup):
+        chain.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        chain.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1000.0 / reps      # seconds per replay
+
+
+def gemv_call(qmm, t, w, y):
+    return lambda: qmm.gemv(t["x"], t["packed"], t["scales"], t["biases"], w.N, w.bits, w.group, out=y)
+
+
+def gemm_call(qmm, t, w, y):
+    return lambda: qmm.gemm(t["x_bf16"], t["packed"], t["scales"], t["biases"], w.N, w.bits, w.group, out=y)
+
+
+def measure_config(name, torch, qmm, stream, pk, reps=20):
+    """Per-launch time of one workload with L2-cold weights (copies > L2)."""
+    w, d, t = device_inputs(name, 0, torch, qmm)
+    if w.prefill:
+        per = w.N * w.K // 2 + w.M * w.K * 2 + w.N * (w.K // w.group) * 4
+    else:
+        per = gemv_bytes(w.M, w.N, w.K, w.bits, w.group)
+    copies = max(2, min(64, -(-4 * l2_bytes(torch) // per)))
+    if w.prefill and w.N * w.K // 2 > l2_bytes(torch):
+        copies = 2
+    ts = replicate(t, copies, torch)
+    ys = [torch.empty((w.M, w.N), dtype=torch.float32, device="cuda") for _ in range(copies)]
+    mk = gemm_call if w.prefill else gemv_call
+    chain = Chain([mk(qmm, ts[i], w, ys[i]) for i in range(copies)], torch).capture(stream)
+    sec = time_graph(chain, reps, 3, torch, stream) / copies
+    out = {"M": w.M, "N": w.N, "K": w.K, "bits": w.bits, "group": w.group, "us_per_launch": sec * 1e6,
+           "copies": copies}
+    if w.prefill:
+        tf = gemm_flops(w.M, w.N, w.K) / sec / 1e12
+        out.update({"tflops": tf, "frac_of_measured_bf16": tf / pk["bf16_tflops"]})
+    else:
+        gbs = gemv_bytes(w.M, w.N, w.K, w.bits, w.group) / sec / 1e9
+        out.update({"gbs": gbs, "frac_of_measured_hbm": gbs / pk["hbm_gbs"],
+                    "frac_of_8tbs": gbs / NOMINAL_HBM_GBS})
+    del ts, ys, chain
+    torch.cuda.empty_cache()
+    return out
+
+
+def traffic_from_profile():
+    """dram bytes per launch of the headline kernel from the committed ncu summary,
+    or None if the summary is missing or the kernel source changed since."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"gemv_source_sha256:\s*([0-9a-f]{16,64})", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
+    if not cur.startswith(h.group(1)):
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(seconds, nthreads=None):
+    """The oracle, as it stands, on whole layers of the headline workload until
+    `seconds` of CPU time have passed (at least one layer).  Returns
+    (bytes processed, elapsed seconds, threads, layers)."""
+    import oracle
+    oracle.build()
+    up, down = inputs.WORKLOADS[HEADLINE_UP], inputs.WORKLOADS[HEADLINE_DOWN]
+    mats = []
+    for w in (up, down):
+        d = inputs.make(w.M, w.N, w.K, w.bits, w.group, 0)
+        mats.append((w, d, oracle.pack(d["codes"], w.bits)))
+    th = nthreads or max(1, len(os.sched_getaffinity(0)))
+    done, layers = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        for w, d, p in mats:
+            oracle.qmm_f32x(d["x"], p, d["scales"], d["biases"], w.N, w.K, w.bits, w.group, nthreads=th)
+            done += gemv_bytes(w.M, w.N, w.K, w.bits, w.group)
+        layers += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done, el, th, layers
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    up, down = inputs.WORKLOADS[HEADLINE_UP], inputs.WORKLOADS[HEADLINE_DOWN]
+    per_layer = gemv_bytes(up.M, up.N, up.K, 4, 64) + gemv_bytes(down.M, down.N, down.K, 4, 64)
+    import oracle
+    oracle.build()
+    mats = []
+    for w in (up, down):
+        d = inputs.make(w.M, w.N, w.K, w.bits, w.group, 0)
+        mats.append((w, d, oracle.pack(d["codes"], w.bits)))
+    th = max(1, len(os.sched_getaffinity(0)))
+
+    def step():
+        for w, d, p in mats:
+            oracle.qmm_f32x(d["x"], p, d["scales"], d["biases"], w.N, w.K, w.bits, w.group, nthreads=th)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    gbs = per_layer * args.steps / el / 1e9
+    sample = (f"{args.steps} steps x one layer (up + down projection, INT4 g64) of the "
+              f"{WORKLOAD_NAME} workload on {th} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "layers_per_step": 1, "seed": 0},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": th, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
+    ap.add_argument("--oracle-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    from quantized_weight_gb300 import build as qbuild
+    from quantized_weight_gb300 import qmm
+
+    qbuild.build()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pk = peaks()
+    stream = torch.cuda.Stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- headline: L layers of up + down projections, weights > 4x L2
+    up_w, up_d, up_t = device_inputs(HEADLINE_UP, 0, torch, qmm)
+    dn_w, dn_d, dn_t = device_inputs(HEADLINE_DOWN, 0, torch, qmm)
+    layer_bytes = (gemv_bytes(1, up_w.N, up_w.K, 4, 64) + gemv_bytes(1, dn_w.N, dn_w.K, 4, 64))
+    layers = max(8, -(-4 * l2_bytes(torch) // layer_bytes))
+    ups, dns = replicate(up_t, layers, torch), replicate(dn_t, layers, torch)
+    y_up = [torch.empty((1, up_w.N), device="cuda") for _ in range(layers)]
+    y_dn = [torch.empty((1, dn_w.N), device="cuda") for _ in range(layers)]
+    calls = []
+    for i in range(layers):
+        calls.append(gemv_call(qmm, ups[i], up_w, y_up[i]))
+        calls.append(gemv_call(qmm, dns[i], dn_w, y_dn[i]))
+    chain = Chain(calls, torch).capture(stream)
+    step_bytes = layers * layer_bytes
+    launches_per_step = 2 * layers
+
+    # parity of the timed configuration, on sampled outputs (carried with the number)
+    import oracle
+    oracle.build()
+    y0 = y_up[0].cpu().numpy()[0]
+    ns = np.arange(0, up_w.N, 97)
+    ref = oracle.qmm_sampled(up_d["x"], oracle.pack(up_d["codes"], 4), up_d["scales"], up_d["biases"],
+                             np.zeros_like(ns), ns, up_w.N, up_w.K, 4, 64)
+    parity = float(np.linalg.norm(y0[ns] - ref) / np.linalg.norm(ref))
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        chain.replay()
+    stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        chain.replay()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    sec = e0.elapsed_time(e1) / 1000.0
+    # keep the same load running long enough for the clock sampler to see it
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            chain.replay()
+        stream.synchronize()
+    clocks = sampler.stop()
+
+    if world > 1:
+        tt = torch.tensor([sec], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        sec = float(tt.item())
+    ms_per_step = sec / args.steps * 1e3
+    value = step_bytes * args.steps * world / sec / 1e9
+    per_launch_s = sec / args.steps / launches_per_step
+    achieved = (step_bytes / launches_per_step) / per_launch_s / 1e9
+
+    # ---- end to end through the public API: host activations in, host results out
+    xs_h = [torch.empty_like(t["x"], device="cpu").pin_memory() for t in ups + dns]
+    for h, t in zip(xs_h, ups + dns):
+        h.copy_(t["x"].cpu())
+    ys_h = [torch.empty_like(y, device="cpu").pin_memory() for y in y_up + y_dn]
+    xs_d = [t["x"] for t in ups + dns]
+    ys_d = y_up + y_dn
+    h2d = sum(h.numel() * 4 for h in xs_h)
+    d2h = sum(h.numel() * 4 for h in ys_h)
+
+    def e2e_step():
+        for h, dtens in zip(xs_h, xs_d):
+            dtens.copy_(h, non_blocking=True)
+        chain.launch_eager()
+        for h, dtens in zip(ys_h, ys_d):
+            h.copy_(dtens, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        f1.record(stream)
+        f1.synchronize()
+        barrier()
+    e2e_sec = f0.elapsed_time(f1) / 1000.0
+    e2e_val = step_bytes * e2e_steps * world / e2e_sec / 1e9
+
+    del chain
+    torch.cuda.empty_cache()
+
+    per_config = {}
+    if not args.no_configs:
+        for name in inputs.WORKLOADS:
+            try:
+                per_config[name] = measure_config(name, torch, qmm, stream, pk)
+            except Exception as ex:        # report, do not hide
+                per_config[name] = {"error": repr(ex)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "layers_per_step": layers, "bytes_per_step": step_bytes,
+                   "launches_per_step": launches_per_step, "seed": 0,
+                   "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of weights per step vs "
+                         f"{l2_bytes(torch) / 1e6:.0f} MB L2, each step reads every code from HBM",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "graph": "CUDA graph per step, programmatic dependent launch between products"},
+        "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
+        "parity": {"sampled_rel_l2_vs_oracle": parity, "tolerance": 1e-5},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic_from_profile(),
+                     "kernel": "gemv_kernel<4,1,8,2,4> (INT4 decode product)",
+                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps,
+                "path": "pinned host x -> device, per-product Python API calls, device y -> pinned host"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "per_config": per_config,
+    }
+    if rank == 0 and world == 1:
+        nbytes, el, th, nl = oracle_sample(args.oracle_seconds)
+        line["cpu_baseline"] = {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle",
+                                "sample": f"{nl} layers (up + down) of {WORKLOAD_NAME}, {el:.1f} s"}
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * qmm.h -- C ABI of libqmm.so: weight-only quantized matrix products on GB300.
+ *
+ *   y = x * dequant(W)^T
+ *
+ * over weights W[N, K] stored as packed low-bit codes with one coefficient
+ * set per group of `group` consecutive elements along K:
+ *
+ *   bits = 4  affine:     w = s * q + b,   q in 0..15
+ *             (group-64 affine INT4 codes with 16-bit scale and bias:
+ *              "Pushing the limits of legacy hardware", section "Start with the
+ *              machine that actually exists"; the formula  q * scale + min  is on
+ *              "I Built an LLM Inference Engine on a 15 year old GPU ...",
+ *              section "Quantization: The Model Doesn't Run on INT4")
+ *   bits = 8  symmetric:  w = s * q,       q a two's-complement int8
+ *             (8-bit group-wise symmetric weights, one scale per group of 64:
+ *              "... Tesla C2075 ..." paper, section 2.3 "Quantization and residency")
+ *   bits = 1  sign:       w = s * (2b - 1), bit b = 1 means +1, b = 0 means -1
+ *             (binary Q1 weights with FP16 scales: "A 27B model on two 4GB
+ *              Maxwell GPUs: inference tuning", section "Why this machine is awkward")
+ *
+ * Layouts (all row-major, all sizes in elements unless stated):
+ *   x       [M, K]  float32 (qmm_gemv) or bfloat16 bit patterns (qmm_gemm)
+ *   codes   [N, K*bits/32] 32-bit words.  Element k of row n sits in word
+ *           k / (32/bits) of that row at bit offset bits * (k mod (32/bits)):
+ *           the lowest nibble / byte / bit holds the lowest k.
+ *   scales  [N, K/group] IEEE binary16 bit patterns
+ *   biases  [N, K/group] IEEE binary16 bit patterns (bits == 4 only, else NULL)
+ *   y       [M, N]  float32, y[m, n] = sum_k x[m, k] * w[n, k]
+ *
+ * Memory and ownership.  Every array argument is device memory owned by the
+ * caller (for instance a torch tensor's storage); the library never keeps a
+ * pointer past the call, and never allocates or frees device memory in any
+ * call (the residency rule of the "15 year old GPU" page, section "Cost 2:
+ * memory is allocated and freed on every layer").  Device pointers must be
+ * 16-byte aligned.
+ *
+ * Asynchrony.  Every call validates its arguments on the host and then only
+ * enqueues kernels on `stream` (a cudaStream_t; NULL is the legacy default
+ * stream) and returns; results are valid once the stream has reached that
+ * point.  On any validation failure nothing is enqueued and no output is
+ * touched ("fail before changing live state": "Pushing the limits of legacy
+ * hardware", section "Build the execution path, then share the weights").
+ *
+ * Errors.  Each call returns a qmm_status.  Launch failures are QMM_ERR_CUDA.
+ * The prefill kernel bounds every wait; if one runs out it records a device
+ * status word and exits without writing its tile, and qmm_check() reports
+ * QMM_ERR_DEVICE_TIMEOUT.  No exception crosses this interface.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qmm_stream_t;   /* the same type as cudaStream_t */
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_ARG = -1,             /* NULL pointer, or a biases pointer that contradicts bits */
+    QMM_ERR_SHAPE = -2,           /* negative size, K % 32, K % group, M outside the entry's range */
+    QMM_ERR_ALIGN = -3,           /* a device pointer not 16-byte aligned */
+    QMM_ERR_UNSUPPORTED = -4,     /* bits / group combination this entry does not implement */
+    QMM_ERR_CUDA = -5,            /* a CUDA runtime call or launch failed */
+    QMM_ERR_DEVICE_TIMEOUT = -6   /* a bounded device-side wait ran out (see qmm_check) */
+} qmm_status;
+
+/*
+ * qmm_pack -- codes one-per-byte -> packed 32-bit words.
+ *   codes  [N, K] uint8: 0..15 (bits 4), the int8 bit pattern (bits 8), 0/1 (bits 1).
+ *          Bits above the format's width are ignored (masked off).
+ *   packed [N, K*bits/32] uint32, written.
+ *   Requires N >= 0, K >= 0, K % 32 == 0, bits in {1, 4, 8}.
+ * Layout: "bits" above.  The pages fix no bit order; this one puts the lowest
+ * k in the lowest bits, as the 4-bit, group-64 shift-and-mask decoder of
+ * "Pushing the limits of legacy hardware" (section "Half a billion values, and
+ * one negative zero") reads codes by shifts and masks.
+ */
+int qmm_pack(const uint8_t *codes, uint32_t *packed, int64_t N, int64_t K, int bits,
+             qmm_stream_t stream);
+
+/*
+ * qmm_unpack -- the inverse of qmm_pack: packed words -> one code per byte
+ * (int8 bit patterns for bits 8, 0/1 for bits 1).  Same requirements.
+ */
+int qmm_unpack(const uint32_t *packed, uint8_t *codes, int64_t N, int64_t K, int bits,
+               qmm_stream_t stream);
+
+/*
+ * qmm_dequant -- dense float32 weights w[N, K] from packed codes.
+ *   w[n, k] = s*q + b (bits 4), s*q (bits 8), s*(2b-1) (bits 1), evaluated in
+ *   float32 with round-to-nearest; s*q is exact in float32, so w is the
+ *   correctly rounded value of the exact weight.  Signed zeros and binary16
+ *   subnormal coefficients are kept (no flush to zero), as the exact-decoder
+ *   work of "Pushing the limits of legacy hardware", section "Half a billion
+ *   values, and one negative zero", requires.
+ *   Requires K % 32 == 0, group > 0, K % group == 0; biases non-NULL iff bits == 4.
+ */
+int qmm_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases,
+                float *w, int64_t N, int64_t K, int bits, int group, qmm_stream_t stream);
+
+/*
+ * qmm_gemv -- decode product y[M, N] = x[M, K] * dequant(W)^T, 1 <= M <= 8.
+ *   float32 activations, float32 accumulation; bandwidth-bound: every code
+ *   is read once from HBM ("... Tesla C2075 ..." paper, section 3.3 "Decode,
+ *   and why 4-bit is slower": decode is a bandwidth-bound matrix-vector
+ *   product reading each weight once).  The reduction order is fixed, so the
+ *   result is the same on every run.  NaN or Inf in x propagate.
+ *   Supported: bits 4 and 8 with group in {32, 64, 128}; bits 1 with group in
+ *   {32, 64, 128} and K % 128 == 0.  K == 0 writes y = 0.
+ *   M == 0 or N == 0 is a no-op.
+ */
+int qmm_gemv(const float *x, const uint32_t *codes, const uint16_t *scales,
+             const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int bits,
+             int group, qmm_stream_t stream);
+
+/*
+ * qmm_gemm -- prefill product y[M, N] = x[M, K] * dequant(W)^T for any M >= 1.
+ *   x holds bfloat16 bit patterns.  Each weight is dequantized in float32,
+ *   rounded to bfloat16 (nearest even) in shared memory, and multiplied on
+ *   the tensor cores with float32 accumulation: the fused replacement of
+ *   "dequantize each weight once into an FP32 scratch buffer, then call the
+ *   vendor GEMM" ("... Tesla C2075 ..." paper, section 3.1 "Prefill
+ *   projections: dequantize, then call the vendor").
+ *   Supported: bits 4, group in {64, 128}, K % 64 == 0, K >= 64.
+ *   M == 0 or N == 0 is a no-op.
+ */
+int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
+             const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int bits,
+             int group, qmm_stream_t stream);
+
+/*
+ * qmm_check -- synchronize `stream`, then report QMM_ERR_CUDA if a kernel
+ * failed, QMM_ERR_DEVICE_TIMEOUT if a bounded wait in a prefill kernel ran
+ * out since the last qmm_check (and clear that record), else QMM_OK.
+ */
+int qmm_check(qmm_stream_t stream);
+
+/* A static, human-readable name for a qmm_status value. */
+const char *qmm_status_string(int status);
+
+/* The ABI version: bumps on any incompatible change of the declarations above. */
+int qmm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMM_H */

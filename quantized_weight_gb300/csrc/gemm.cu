@@ -1,0 +1,449 @@
+// gemm.cu -- the prefill product y[M, N] = x[M, K] * dequant(W)^T on tcgen05.
+//
+// The page of the "... Tesla C2075 ..." paper (section 3.1 "Prefill projections:
+// dequantize, then call the vendor") dequantizes every 8-bit weight into an FP32
+// scratch matrix and then calls the vendor GEMM; the Maxwell Q1 page ("A 27B
+// model on two 4GB Maxwell GPUs", section "A packed Q1 prefill kernel with a
+// narrow dispatch window") expands Q1 weights to FP32 before SGEMM.  Here the
+// dequantization is fused into the tensor-core pipeline instead: codes travel
+// from HBM to shared memory by TMA, four warps turn each 128-row x 64-k code
+// tile into bf16 directly in the 128-byte-swizzled K-major layout the tensor
+// core reads, and no dequantized weight ever reaches global memory.
+//
+// Roles of one persistent CTA per SM (10 warps):
+//   warp 0      TMA producer: per K-step, the x tile (bf16, BN tokens x 64 k,
+//               128-byte swizzle) and the code tile (128 rows x 32 bytes)
+//   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
+//   warps 2-5   dequantization: thread t owns weight row t of the tile:
+//               w = s*q + b in float32 (exact products, one rounding), then
+//               round-to-nearest-even bf16, stored swizzled, proxy-fenced
+//   warps 6-9   epilogue: tcgen05.ld of the f32 accumulator, y stored with
+//               32 consecutive n per warp-wide store
+//
+// The MMA computes D[128 weight rows, BN tokens] = A * B^T with A = the
+// dequantized weight tile and B = the x tile, i.e. the transpose of a y tile;
+// putting the weights on the M side lets one dequantized tile serve BN tokens.
+// Two accumulators of BN columns live in TMEM so the epilogue of one tile
+// overlaps the main loop of the next.  Stage buffers are guarded by mbarriers
+// (TMA -> full, dequant -> afull, MMA commit -> empty).
+//
+// Every wait is bounded by wall time (globaltimer).  A wait that runs out
+// records QMM_ERR_DEVICE_TIMEOUT in a device status word, raises a CTA-wide
+// abort flag that the other roles poll, drains this CTA's outstanding TMA
+// copies and MMAs (again with bounded waits), frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "qmm_device.cuh"
+#include "qmm_launch.h"
+#include "sm100_ptx.cuh"
+
+namespace qmm {
+
+__device__ int g_device_status = 0;   // QMM_OK or QMM_ERR_DEVICE_TIMEOUT (-6)
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;                // weight rows per tile (MMA M)
+constexpr int BK = 64;                 // k per stage: one 128-byte swizzle atom of bf16
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;
+constexpr int NUM_THREADS = 320;
+constexpr int DQ_WARP0 = 2, EPI_WARP0 = 6;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: any legitimate wait is far shorter
+constexpr int kTimeoutStatus = -6;
+
+template <int BN>
+struct Smem {
+  static constexpr int A_BYTES = BM * BK * 2;      // 16 KB dequantized weights (bf16)
+  static constexpr int B_BYTES = BN * BK * 2;      // x tile (bf16)
+  static constexpr int C_BYTES = BM * BK / 2;      // 4 KB codes
+  static constexpr int STAGE = A_BYTES + B_BYTES + C_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE;   // multiple of 1024
+  static constexpr int BARS = 3 * STAGES + 4 + 1;  // full, afull, empty, acc_full[2], acc_empty[2], drain
+  static constexpr int TOTAL = BAR_OFF + BARS * 8 + 16 /* tmem slot + abort flag */;
+  static constexpr int ALLOC = TOTAL + 1024;       // slack to align the base to 1024
+  static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                        : (2 * BN <= 256) ? 256 : 512;
+};
+
+struct GemmParams {
+  const uint16_t *scales;
+  const uint16_t *biases;
+  float *y;
+  int M, N, K;
+  int gshift;
+  int groups_per_row;
+  int m_blocks, n_blocks, tiles;
+};
+
+struct Ctl {
+  volatile int *abort;
+};
+
+// Bounded wait.  Returns false (after recording the timeout) if the phase did
+// not complete within the limit, or if another role of this CTA aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl &ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; it++) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*ctl.abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *ctl.abort = 1;
+        atomicExch(&g_device_status, kTimeoutStatus);
+        return false;
+      }
+    }
+  }
+}
+
+// Waits used only while draining after an abort: bounded, never raise.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+}
+
+// Dequantize 8 codes (one 32-bit word, k = 8c .. 8c+7) into 8 bf16 packed as
+// four 32-bit words, k order low-to-high within each word.
+//   w_j = s*q_j + b, evaluated as fma(s*16^-cls, q_j*16^cls, b): the nibble is
+//   masked in place and OR-ed into the bits of 2^23 (an exact float
+//   2^23 + q*16^cls), 2^23 is subtracted exactly, and the power-of-two
+//   pre-scaled s makes the product exact, so the FMA rounds s*q + b once.
+__device__ __forceinline__ uint4 dequant_word_bf16(uint32_t w, const f2 (&sp)[4], f2 b2) {
+  const f2 magic2 = f2_make(8388608.0f, 8388608.0f);
+  const uint32_t wh = w >> 12;
+  const uint32_t M0 = 0x4B000000u;
+  f2 q01 = f2_sub(f2_bits(and_or(w, 0xFu, M0), and_or(w, 0xF0u, M0)), magic2);
+  f2 q23 = f2_sub(f2_bits(and_or(w, 0xF00u, M0), and_or(w, 0xF000u, M0)), magic2);
+  f2 q45 = f2_sub(f2_bits(and_or(w, 0xF0000u, M0), and_or(wh, 0xF00u, M0)), magic2);
+  f2 q67 = f2_sub(f2_bits(and_or(wh, 0xF000u, M0), and_or(wh, 0xF0000u, M0)), magic2);
+  // sp[0] = (s, s/16), sp[1] = (s/256, s/4096), sp[2] = (s/65536, s/256), sp[3] = (s/4096, s/65536)
+  f2 v01 = f2_fma(q01, sp[0], b2);
+  f2 v23 = f2_fma(q23, sp[1], b2);
+  f2 v45 = f2_fma(q45, sp[2], b2);
+  f2 v67 = f2_fma(q67, sp[3], b2);
+  float a, c;
+  uint4 o;
+  f2_split(v01, a, c);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(c), "f"(a));
+  f2_split(v23, a, c);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(c), "f"(a));
+  f2_split(v45, a, c);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(c), "f"(a));
+  f2_split(v67, a, c);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(c), "f"(a));
+  return o;
+}
+
+__device__ __forceinline__ void scale_pairs(float s, f2 (&sp)[4]) {
+  const float s1 = s * 0.0625f, s2 = s * 0.00390625f, s3 = s * 0.000244140625f,
+              s4 = s * 1.52587890625e-05f;   // exact: powers of two, no underflow for binary16 s
+  sp[0] = f2_make(s, s1);
+  sp[1] = f2_make(s2, s3);
+  sp[2] = f2_make(s4, s2);
+  sp[3] = f2_make(s3, s4);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    qmm_gemm_int4_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                         const __grid_constant__ CUtensorMap tmap_codes, const GemmParams p) {
+  using S = Smem<BN>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // align the working area to 1024 bytes (128-byte swizzle atoms)
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  auto a_buf = [&](int s) { return sbase + s * S::STAGE; };
+  auto b_buf = [&](int s) { return sbase + s * S::STAGE + S::A_BYTES; };
+  auto c_ptr = [&](int s) { return smem + s * S::STAGE + S::A_BYTES + S::B_BYTES; };
+  auto c_buf = [&](int s) { return sbase + s * S::STAGE + S::A_BYTES + S::B_BYTES; };
+  const uint32_t bars = sbase + S::BAR_OFF;
+  auto full = [&](int s) { return bars + 8 * s; };
+  auto afull = [&](int s) { return bars + 8 * (STAGES + s); };
+  auto empty = [&](int s) { return bars + 8 * (2 * STAGES + s); };
+  auto acc_full = [&](int b) { return bars + 8 * (3 * STAGES + b); };
+  auto acc_empty = [&](int b) { return bars + 8 * (3 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8 * (3 * STAGES + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::BAR_OFF + S::BARS * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::BAR_OFF + S::BARS * 8 + 4);
+  const Ctl ctl{abort_flag};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ksteps = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; s++) {
+      mbar_init(full(s), 1);
+      mbar_init(afull(s), 128);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), S::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_x);
+      tma_prefetch_desc(&tmap_codes);
+      int it = 0;                   // global K-step counter of this CTA
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        const int mb = tile % p.m_blocks, nb = tile / p.m_blocks;
+        for (int kb = 0; kb < ksteps; kb++, it++) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
+          mbar_arrive_expect_tx(full(s), S::B_BYTES + S::C_BYTES);
+          tma_load_2d(b_buf(s), &tmap_x, kb * BK, mb * BN, full(s));
+          tma_load_2d(c_buf(s), &tmap_codes, kb * (BK / 2), nb * BM, full(s));
+        }
+      }
+      if (!ok) {
+        // drain: every copy this thread issued must land before the CTA exits
+        const int first = it > STAGES ? it - STAGES : 0;
+        for (int j = first; j < it; j++) wait_drain(full(j % STAGES), (j / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, local++) {
+        const int buf = local & 1;
+        const uint32_t use = (local >> 1) & 1;
+        if (!wait_bounded(acc_empty(buf), use ^ 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < ksteps; kb++, it++) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!wait_bounded(full(s), ph, ctl) || !wait_bounded(afull(s), ph, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(a_buf(s));
+          const uint64_t bd = smem_desc_sw128(b_buf(s));
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; kk++) {
+            // +32 bytes per 16 k inside the swizzle atom: +2 in the encoded address
+            umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          }
+          umma_commit(empty(s));          // stage free once these MMAs have read it
+        }
+        if (!ok) break;
+        umma_commit(acc_full(buf));       // accumulator complete
+      }
+      if (!ok) {
+        umma_commit(drain_bar);           // wait for every MMA issued so far
+        wait_drain(drain_bar, 0);
+      }
+    }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ dequantization
+    const int t = threadIdx.x - DQ_WARP0 * 32;      // weight row within the tile
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+      const int nb = tile / p.m_blocks;
+      const int row = nb * BM + t;
+      const bool row_ok = row < p.N;
+      const uint16_t *srow = p.scales + (int64_t)(row_ok ? row : 0) * p.groups_per_row;
+      const uint16_t *brow = p.biases + (int64_t)(row_ok ? row : 0) * p.groups_per_row;
+      // coefficients of K-steps kb, kb+1, kb+2 in flight (rotating registers)
+      uint16_t s0 = 0, b0 = 0, s1 = 0, b1 = 0, s2 = 0, b2v = 0;
+      if (row_ok) {
+        s0 = ld_nc_u16(srow + ((0 * BK) >> p.gshift));
+        b0 = ld_nc_u16(brow + ((0 * BK) >> p.gshift));
+        if (ksteps > 1) { s1 = ld_nc_u16(srow + ((1 * BK) >> p.gshift)); b1 = ld_nc_u16(brow + ((1 * BK) >> p.gshift)); }
+        if (ksteps > 2) { s2 = ld_nc_u16(srow + ((2 * BK) >> p.gshift)); b2v = ld_nc_u16(brow + ((2 * BK) >> p.gshift)); }
+      }
+      for (int kb = 0; kb < ksteps; kb++, it++) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        uint16_t s3 = 0, b3 = 0;
+        if (row_ok && kb + 3 < ksteps) {
+          s3 = ld_nc_u16(srow + (((kb + 3) * BK) >> p.gshift));
+          b3 = ld_nc_u16(brow + (((kb + 3) * BK) >> p.gshift));
+        }
+        const float sf = row_ok ? h2f(s0) : 0.0f;
+        const float bf = row_ok ? h2f(b0) : 0.0f;
+        if (!wait_bounded(full(s), ph, ctl)) { ok = false; break; }
+        const uint4 *cw = reinterpret_cast<const uint4 *>(c_ptr(s) + t * 32);
+        const uint4 lo = cw[0], hi = cw[1];
+        f2 sp[4];
+        scale_pairs(sf, sp);
+        const f2 bb = f2_make(bf, bf);
+        const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        const uint32_t arow = a_buf(s) + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          const uint4 v = dequant_word_bf16(words[c], sp, bb);
+          const uint32_t dst = arow + ((c ^ (t & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                       "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(afull(s));
+        s0 = s1; b0 = b1; s1 = s2; b1 = b2v; s2 = s3; b2v = b3;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                          // TMEM lane quarter this warp may read
+    const int r = q * 32 + lane;                     // weight row within the tile
+    int local = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, local++) {
+      const int mb = tile % p.m_blocks, nb = tile / p.m_blocks;
+      const int buf = local & 1;
+      const uint32_t use = (local >> 1) & 1;
+      if (!wait_bounded(acc_full(buf), use, ctl)) { ok = false; break; }
+      tc_fence_after();
+      const int n = nb * BM + r;
+      const int m0 = mb * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + c0, v);
+        tmem_ld_wait();
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; j++) {
+            const int m = m0 + c0 + j;
+            if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+int sm_count_gemm() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+template <int BN>
+cudaError_t launch_bn(const uint16_t *x_bf16, const uint32_t *codes, const GemmParams &p0,
+                      cudaStream_t s) {
+  using S = Smem<BN>;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tx, tc;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)p0.K, (cuuint64_t)p0.M};
+    cuuint64_t strides[1] = {(cuuint64_t)p0.K * 2};
+    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x_bf16), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)p0.K / 2, (cuuint64_t)p0.N};
+    cuuint64_t strides[1] = {(cuuint64_t)p0.K / 2};
+    cuuint32_t box[2] = {BK / 2, BM};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(codes), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  GemmParams p = p0;
+  p.m_blocks = (p.M + BN - 1) / BN;
+  p.n_blocks = (p.N + BM - 1) / BM;
+  p.tiles = p.m_blocks * p.n_blocks;
+  auto kern = qmm_gemm_int4_kernel<BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+  if (e != cudaSuccess) return e;
+  const int grid = p.tiles < sm_count_gemm() ? p.tiles : sm_count_gemm();
+  kern<<<grid, NUM_THREADS, S::ALLOC, s>>>(tx, tc, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
+                        const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int group,
+                        cudaStream_t s) {
+  GemmParams p{};
+  p.scales = scales;
+  p.biases = biases;
+  p.y = y;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.gshift = __builtin_ctz((unsigned)group);
+  p.groups_per_row = (int)(K / group);
+  if (M > 128) return launch_bn<256>(x_bf16, codes, p, s);
+  if (M > 64) return launch_bn<128>(x_bf16, codes, p, s);
+  return launch_bn<64>(x_bf16, codes, p, s);
+}
+
+cudaError_t read_and_clear_device_status(int *status, cudaStream_t s) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_device_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+  }
+  *status = v;
+  return cudaSuccess;
+}
+
+}  // namespace qmm

@@ -1,0 +1,167 @@
+// pack.cu -- pack / unpack / dequantize kernels.
+//
+// Packing convention (the pages fix no bit order): element k of a row sits in
+// 32-bit word k / (32/bits) of that row, at bit offset bits * (k mod (32/bits)),
+// lowest k in the lowest bits -- the order a shift-and-mask decoder of
+// group-64 4-bit codes reads ("Pushing the limits of legacy hardware", section
+// "Half a billion values, and one negative zero").  Rows are K*bits/32 words
+// long with no padding, so word i of the whole matrix holds the codes of
+// elements [i*(32/bits), (i+1)*(32/bits)) of the flattened [N, K] array: the
+// pack and unpack kernels need no row arithmetic.
+//
+// One thread handles one 32-bit word in a grid-stride loop; reads and writes
+// are contiguous across consecutive threads.
+#include "qmm_device.cuh"
+#include "qmm_launch.h"
+
+namespace qmm {
+namespace {
+
+constexpr int kThreads = 256;
+
+int grid_for(int64_t items) {
+  int64_t blocks = (items + kThreads - 1) / kThreads;
+  if (blocks > 152 * 16) blocks = 152 * 16;   // grid-stride beyond 16 blocks per SM
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) pack_kernel(const uint8_t *__restrict__ codes,
+                                                         uint32_t *__restrict__ packed,
+                                                         int64_t words) {
+  constexpr int PER = 32 / BITS;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint8_t *c = codes + i * PER;
+    uint32_t w = 0;
+    if (BITS == 8) {
+      w = *reinterpret_cast<const uint32_t *>(c);          // already 4 bytes in k order
+    } else if (BITS == 4) {
+      uint2 b = *reinterpret_cast<const uint2 *>(c);        // 8 codes, one per byte
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        w |= ((b.x >> (8 * j)) & MASK) << (4 * j);
+        w |= ((b.y >> (8 * j)) & MASK) << (4 * (j + 4));
+      }
+    } else {
+      const uint4 *c4 = reinterpret_cast<const uint4 *>(c);  // 32 codes, one per byte
+      uint4 lo = c4[0], hi = c4[1];
+      uint32_t b[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int q = 0; q < 8; q++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) w |= ((b[q] >> (8 * j)) & 1u) << (4 * q + j);
+    }
+    packed[i] = w;
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) unpack_kernel(const uint32_t *__restrict__ packed,
+                                                           uint8_t *__restrict__ codes,
+                                                           int64_t words) {
+  constexpr int PER = 32 / BITS;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t w = packed[i];
+    uint8_t *c = codes + i * PER;
+    if (BITS == 8) {
+      *reinterpret_cast<uint32_t *>(c) = w;
+    } else if (BITS == 4) {
+      uint2 b = make_uint2(0, 0);
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        b.x |= ((w >> (4 * j)) & MASK) << (8 * j);
+        b.y |= ((w >> (4 * (j + 4))) & MASK) << (8 * j);
+      }
+      *reinterpret_cast<uint2 *>(c) = b;
+    } else {
+      uint32_t b[8];
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        b[q] = 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) b[q] |= ((w >> (4 * q + j)) & 1u) << (8 * j);
+      }
+      uint4 *c4 = reinterpret_cast<uint4 *>(c);
+      c4[0] = make_uint4(b[0], b[1], b[2], b[3]);
+      c4[1] = make_uint4(b[4], b[5], b[6], b[7]);
+    }
+  }
+}
+
+// w = s*q + b (bits 4), s*q (bits 8), s*(2b-1) (bits 1), in float32 with
+// round-to-nearest.  s*q is exact in float32 (at most 11 + 8 significant
+// bits), so a single rounded add gives the correctly rounded weight; the
+// explicit _rn intrinsics keep the compiler from contracting or reordering.
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(
+    const uint32_t *__restrict__ packed, const uint16_t *__restrict__ scales,
+    const uint16_t *__restrict__ biases, float *__restrict__ out, int64_t words,
+    int64_t words_per_row, int64_t groups_per_row, int group) {
+  constexpr int PER = 32 / BITS;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < words;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t n = i / words_per_row;
+    int64_t k0 = (i % words_per_row) * PER;
+    int64_t gi = n * groups_per_row + k0 / group;   // a word never straddles a group
+    float s = h2f(scales[gi]);
+    float b = (BITS == 4) ? h2f(biases[gi]) : 0.0f;
+    uint32_t w = packed[i];
+    float v[PER];
+#pragma unroll
+    for (int j = 0; j < PER; j++) {
+      uint32_t u = (w >> (BITS * j)) & ((1u << BITS) - 1u);
+      if (BITS == 4) {
+        v[j] = __fadd_rn(__fmul_rn(s, (float)u), b);
+      } else if (BITS == 8) {
+        v[j] = __fmul_rn(s, (float)(int)(int8_t)(uint8_t)u);
+      } else {
+        v[j] = u ? s : -s;                            // s * (2b - 1), exact
+      }
+    }
+    float4 *o = reinterpret_cast<float4 *>(out + i * PER);
+#pragma unroll
+    for (int j = 0; j < PER / 4; j++) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const uint8_t *codes, uint32_t *packed, int64_t N, int64_t K, int bits,
+                        cudaStream_t s) {
+  int64_t words = N * K * bits / 32;
+  if (words == 0) return cudaSuccess;
+  int g = grid_for(words);
+  if (bits == 4) pack_kernel<4><<<g, kThreads, 0, s>>>(codes, packed, words);
+  else if (bits == 8) pack_kernel<8><<<g, kThreads, 0, s>>>(codes, packed, words);
+  else pack_kernel<1><<<g, kThreads, 0, s>>>(codes, packed, words);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const uint32_t *packed, uint8_t *codes, int64_t N, int64_t K, int bits,
+                          cudaStream_t s) {
+  int64_t words = N * K * bits / 32;
+  if (words == 0) return cudaSuccess;
+  int g = grid_for(words);
+  if (bits == 4) unpack_kernel<4><<<g, kThreads, 0, s>>>(packed, codes, words);
+  else if (bits == 8) unpack_kernel<8><<<g, kThreads, 0, s>>>(packed, codes, words);
+  else unpack_kernel<1><<<g, kThreads, 0, s>>>(packed, codes, words);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases,
+                           float *w, int64_t N, int64_t K, int bits, int group, cudaStream_t s) {
+  int64_t words = N * K * bits / 32;
+  if (words == 0) return cudaSuccess;
+  int64_t wpr = K * bits / 32, gpr = K / group;
+  int g = grid_for(words);
+  if (bits == 4) dequant_kernel<4><<<g, kThreads, 0, s>>>(packed, scales, biases, w, words, wpr, gpr, group);
+  else if (bits == 8) dequant_kernel<8><<<g, kThreads, 0, s>>>(packed, scales, biases, w, words, wpr, gpr, group);
+  else dequant_kernel<1><<<g, kThreads, 0, s>>>(packed, scales, biases, w, words, wpr, gpr, group);
+  return cudaGetLastError();
+}
+
+}  // namespace qmm

@@ -1,0 +1,32 @@
+// qmm_launch.h -- internal launchers behind the C ABI (include/qmm.h).
+//
+// The ABI layer (api.cu) validates every argument before calling one of
+// these; each launcher only picks a kernel configuration and enqueues it on
+// the given stream, returning the cudaError_t of the launch.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmm {
+
+cudaError_t launch_pack(const uint8_t *codes, uint32_t *packed, int64_t N, int64_t K, int bits,
+                        cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t *packed, uint8_t *codes, int64_t N, int64_t K, int bits,
+                          cudaStream_t s);
+cudaError_t launch_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases,
+                           float *w, int64_t N, int64_t K, int bits, int group, cudaStream_t s);
+
+// Decode product, 1 <= M <= 8, K > 0, N > 0.
+cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *scales,
+                        const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits,
+                        int group, cudaStream_t s);
+
+// Prefill product, bits == 4, group in {64, 128}, K % 64 == 0, M >= 1, N >= 1.
+cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
+                        const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K,
+                        int group, cudaStream_t s);
+
+// Device status word written by kernels whose bounded waits ran out.
+cudaError_t read_and_clear_device_status(int *status, cudaStream_t s);
+
+}  // namespace qmm

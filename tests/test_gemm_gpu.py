@@ -1,0 +1,83 @@
+"""GPU prefill product (tcgen05) against the FP64 oracle on the same bf16 x:
+max per-row relative L2 <= 5e-3."""
+import numpy as np
+import pytest
+
+from quantized_weight_gb300 import inputs
+from helpers import rel_l2_rows, to_device
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_weight_gb300 import build, qmm as q
+    build.build()
+    return q
+
+
+SHAPES = [  # M, N, K, group: single and several tiles, ragged M and N, every BN variant
+    (1, 128, 64, 64), (7, 200, 128, 64), (64, 256, 2048, 64), (100, 300, 1024, 128),
+    (129, 1000, 512, 64), (256, 384, 2048, 64), (300, 130, 256, 64), (513, 1024, 2048, 64),
+    (1024, 640, 1024, 128),
+]
+
+
+@pytest.mark.parametrize("M,N,K,group", SHAPES)
+def test_small_shapes(qmm, oracle_mod, M, N, K, group):
+    d = inputs.make(M, N, K, 4, group, seed=M + N + K, prefill=True)
+    t = to_device(d, 4, with_bf16=True)
+    p = qmm.pack(t["codes"], 4)
+    y = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], N, 4, group)
+    qmm.check()
+    y = y.cpu().numpy()
+    ref = oracle_mod.qmm_bf16x(d["x_bf16"], oracle_mod.pack(d["codes"], 4), d["scales"], d["biases"],
+                              N, K, 4, group)
+    err = rel_l2_rows(y, ref)
+    assert err <= TOL, (M, N, K, group, err)
+
+
+@pytest.mark.parametrize("name", ["prefill_int4_m1024_k2048_n6144", "prefill_int4_m256_k2048_n151936"])
+def test_full_size_sampled(qmm, oracle_mod, name):
+    w = inputs.WORKLOADS[name]
+    d = inputs.make_workload(name)
+    t = to_device(d, 4, with_bf16=True)
+    p = qmm.pack(t["codes"], 4)
+    y = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, 4, w.group)
+    qmm.check()
+    rng = np.random.default_rng(123)
+    rows = rng.choice(w.M, size=min(48, w.M), replace=False)
+    cols = np.concatenate([rng.choice(w.N, size=60, replace=False), [0, w.N - 1]])
+    ms, ns = np.repeat(rows, cols.size), np.tile(cols, rows.size)
+    ref = oracle_mod.qmm_sampled(d["x_bf16"], oracle_mod.pack(d["codes"], 4), d["scales"], d["biases"],
+                                 ms, ns, w.N, w.K, 4, w.group).reshape(rows.size, cols.size)
+    got = y[torch_index(rows), :][:, torch_index(cols)].cpu().numpy()
+    # relative L2 over the sampled entries of each row estimates the row's relative L2
+    assert rel_l2_rows(got, ref) <= TOL
+    y2 = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, 4, w.group)
+    import torch
+    assert torch.equal(y, y2)                    # same bits on every run
+
+
+def torch_index(a):
+    import torch
+    return torch.as_tensor(np.asarray(a), device="cuda", dtype=torch.long)
+
+
+def test_nan_in_x_propagates_to_its_row_only(qmm):
+    M, N, K = 5, 256, 256
+    d = inputs.make(M, N, K, 4, 64, seed=9, prefill=True)
+    d["x_bf16"][2, 100] = 0x7FC0                   # bf16 NaN
+    t = to_device(d, 4, with_bf16=True)
+    p = qmm.pack(t["codes"], 4)
+    y = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], N, 4, 64).cpu().numpy()
+    assert np.isnan(y[2]).all()
+    assert np.isfinite(np.delete(y, 2, axis=0)).all()
+
+
+def test_check_reports_ok_after_normal_runs(qmm):
+    qmm.check()
