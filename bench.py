@@ -171,6 +171,7 @@ class Chain:
         self.calls = calls
         self.torch = torch
         self.graph = None
+        self.stream = None
 
     def launch_eager(self):
         for c in self.calls:
@@ -185,10 +186,13 @@ class Chain:
         with torch.cuda.graph(g, stream=stream):
             self.launch_eager()
         self.graph = g
+        self.stream = stream
         return self
 
     def replay(self):
-        self.graph.replay()
+        # a graph launches on the current stream: make that the timed stream
+        with self.torch.cuda.stream(self.stream):
+            self.graph.replay()
 
 
 def time_graph(chain, reps, warmup, torch, stream):
@@ -330,6 +334,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
+    ap.add_argument("--no-clock-load", action="store_true",
+                    help="skip the 1 s sustained replay after the timed region (for profiler runs)")
+    ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -398,7 +405,7 @@ def main():
     barrier()
     sec = e0.elapsed_time(e1) / 1000.0
     # keep the same load running long enough for the clock sampler to see it
-    t_end = time.perf_counter() + 1.0
+    t_end = time.perf_counter() + (0.0 if args.no_clock_load else 1.0)
     while time.perf_counter() < t_end:
         for _ in range(50):
             chain.replay()
@@ -431,7 +438,7 @@ def main():
         for h, dtens in zip(ys_h, ys_d):
             h.copy_(dtens, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 50))
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
     with torch.cuda.stream(stream):
         for _ in range(3):
             e2e_step()

@@ -34,13 +34,14 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "bounded_wait.cuh"
 #include "qmm_device.cuh"
 #include "qmm_launch.h"
 #include "sm100_ptx.cuh"
 
 namespace qmm {
 
-__device__ int g_device_status = 0;   // QMM_OK or QMM_ERR_DEVICE_TIMEOUT (-6)
+__device__ int g_gemm_status = 0;   // QMM_OK or QMM_ERR_DEVICE_TIMEOUT (-6)
 
 namespace {
 
@@ -52,8 +53,6 @@ constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
 constexpr int NUM_THREADS = 320;
 constexpr int DQ_WARP0 = 2, EPI_WARP0 = 6;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: any legitimate wait is far shorter
-constexpr int kTimeoutStatus = -6;
 
 template <int BN>
 struct Smem {
@@ -78,35 +77,6 @@ struct GemmParams {
   int groups_per_row;
   int m_blocks, n_blocks, tiles;
 };
-
-struct Ctl {
-  volatile int *abort;
-};
-
-// Bounded wait.  Returns false (after recording the timeout) if the phase did
-// not complete within the limit, or if another role of this CTA aborted.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl &ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; it++) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*ctl.abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *ctl.abort = 1;
-        atomicExch(&g_device_status, kTimeoutStatus);
-        return false;
-      }
-    }
-  }
-}
-
-// Waits used only while draining after an abort: bounded, never raise.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-}
 
 // Dequantize 8 codes (one 32-bit word, k = 8c .. 8c+7) into 8 bf16 packed as
 // four 32-bit words, k order low-to-high within each word.
@@ -172,7 +142,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t drain_bar = bars + 8 * (3 * STAGES + 4);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::BAR_OFF + S::BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::BAR_OFF + S::BARS * 8 + 4);
-  const Ctl ctl{abort_flag};
+  const WaitCtl ctl{abort_flag, &g_gemm_status};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ksteps = p.K / BK;
@@ -429,15 +399,15 @@ cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uin
   return launch_bn<64>(x_bf16, codes, p, s);
 }
 
-cudaError_t read_and_clear_device_status(int *status, cudaStream_t s) {
+cudaError_t read_clear_gemm_status(int *status, cudaStream_t s) {
   int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_device_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_gemm_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return e;
   e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return e;
   if (v != 0) {
     const int zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    e = cudaMemcpyToSymbolAsync(g_gemm_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return e;
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;

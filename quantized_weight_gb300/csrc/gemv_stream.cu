@@ -1,0 +1,468 @@
+// gemv_stream.cu -- decode product y[1, N] = x[1, K] * dequant(W)^T, fed by the TMA engine.
+//
+// Decode reads each weight once and is bound by memory bandwidth ("... Tesla
+// C2075 ..." paper, section 3.3 "Decode, and why 4-bit is slower").  At GB300's
+// bandwidth a decode-sized matrix (a few MB) must be almost entirely in flight
+// at once to keep HBM busy, which registers cannot hold.  So each CTA (one per
+// SM) owns a contiguous slab of rows and one producer thread streams the slab
+// into shared memory with a handful of large bulk async copies (the TMA
+// engine; completion counted on mbarriers): the coefficients of all the slab's
+// rows, then the codes in stages of up to 16 rows.  The weights do not depend
+// on the previous kernel in the stream, so the producer runs before the
+// programmatic-dependent-launch wait and a chain of decode products keeps HBM
+// streaming across kernel boundaries.
+//
+// After that wait, the consumer warps load x once per CTA with coalesced
+// loads into a transposed shared-memory layout; each warp then owns one
+// K-segment (32 lanes x 16 bytes of codes: 1024 INT4, 512 INT8 or, with 4-byte
+// lanes, 1024 Q1 weights) and keeps that segment's activations in registers.
+// A warp takes every wps-th group of 4 rows of the slab; per group the lanes
+// form partial dot products with exact bit tricks (below), a transposing
+// butterfly reduces the 4 rows over the warp (6 shuffles), and the totals go to
+// a per-row, per-segment slot in shared memory.  When every warp is done, one
+// thread per row adds the segment slots in segment order and stores y: no
+// atomics, the same bits on every run.
+//
+//   INT4  q*16^c comes out of one lop3 (the masked nibble, left where it sits
+//         in the word, OR-ed into the bits of 2^23) and one packed f32x2
+//         subtract; nibble pairs of equal position class share a packed FMA
+//         accumulator; the group bias is factored out as b * sum(x).
+//   INT8  after XOR 0x80 per byte, one prmt builds the float 2^23 + (q + 128).
+//   Q1    w*x = +-x: one shift and one lop3 move the sign bit.
+//
+// Every mbarrier wait is bounded (bounded_wait.cuh); a wait that runs out
+// aborts the CTA, drains its outstanding copies and records
+// QMM_ERR_DEVICE_TIMEOUT for qmm_check().
+#include "bounded_wait.cuh"
+#include "qmm_device.cuh"
+#include "qmm_launch.h"
+#include "sm100_ptx.cuh"
+
+namespace qmm {
+
+__device__ int g_gemv_status = 0;
+
+namespace {
+
+using namespace sm100;
+
+constexpr uint32_t kMagic = 0x4B000000u;   // bit pattern of 2^23
+constexpr int RG = 4;                      // rows per group (one butterfly)
+constexpr int STAGE_ROWS_MAX = 16;         // rows per code stage
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxConsumerWarps = 15;
+
+template <int BITS>
+struct Lane {
+  static constexpr int BYTES = BITS == 1 ? 4 : 16;     // codes per lane per row
+  static constexpr int W = BYTES * 8 / BITS;           // weights per lane per row
+  static constexpr int SEG_W = 32 * W;                 // weights per warp segment
+  static constexpr int SEG_BYTES = 32 * BYTES;
+  static constexpr int PAIRS = W / 2;                  // x register pairs per lane
+};
+
+struct StreamParams {
+  const float *x;
+  const uint8_t *codes;
+  const uint16_t *scales;
+  const uint16_t *biases;
+  float *y;
+  int N, K, G, gshift;
+  int row_bytes;       // K * bits / 8
+  int segs;            // K / SEG_W
+  int wps;             // consumer warps per K-segment
+  int stage_rows;      // rows per code stage (multiple of RG)
+  int stages;          // ring depth
+  int rows_per_cta;
+  // shared-memory layout (bytes from the 128-byte-aligned base)
+  int off_coef, off_x, off_red, off_bar;
+};
+
+// INT4, two rows at once; see the file comment.  x pairs per word:
+// (x0,x1) (x2,x3) (x5,x6) (x4,x7).
+__device__ __forceinline__ void dot2_int4(const uint4 ca, const uint4 cb, const f2 (&xp)[16], float &da,
+                                          float &db) {
+  const f2 magic2 = f2_make(8388608.0f, 8388608.0f);
+  f2 aA = f2_zero(), aB = f2_zero(), aC = f2_zero();
+  f2 bA = f2_zero(), bB = f2_zero(), bC = f2_zero();
+  const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+  const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+  for (int wi = 0; wi < 4; wi++) {
+    const uint32_t w = wa[wi], wh = w >> 12;
+    const uint32_t v = wb[wi], vh = v >> 12;
+    const f2 x01 = xp[4 * wi + 0], x23 = xp[4 * wi + 1], x56 = xp[4 * wi + 2], x47 = xp[4 * wi + 3];
+    aA = f2_fma(f2_sub(f2_bits(and_or(w, 0xFu, kMagic), and_or(w, 0xF0u, kMagic)), magic2), x01, aA);
+    bA = f2_fma(f2_sub(f2_bits(and_or(v, 0xFu, kMagic), and_or(v, 0xF0u, kMagic)), magic2), x01, bA);
+    aB = f2_fma(f2_sub(f2_bits(and_or(w, 0xF00u, kMagic), and_or(w, 0xF000u, kMagic)), magic2), x23, aB);
+    bB = f2_fma(f2_sub(f2_bits(and_or(v, 0xF00u, kMagic), and_or(v, 0xF000u, kMagic)), magic2), x23, bB);
+    aC = f2_fma(f2_sub(f2_bits(and_or(w, 0xF0000u, kMagic), and_or(wh, 0xF0000u, kMagic)), magic2), x47, aC);
+    bC = f2_fma(f2_sub(f2_bits(and_or(v, 0xF0000u, kMagic), and_or(vh, 0xF0000u, kMagic)), magic2), x47, bC);
+    aB = f2_fma(f2_sub(f2_bits(and_or(wh, 0xF00u, kMagic), and_or(wh, 0xF000u, kMagic)), magic2), x56, aB);
+    bB = f2_fma(f2_sub(f2_bits(and_or(vh, 0xF00u, kMagic), and_or(vh, 0xF000u, kMagic)), magic2), x56, bB);
+  }
+  float t0, t1;
+  f2_split(aA, t0, t1);
+  float d = fmaf(t1, 0.0625f, t0);
+  f2_split(aB, t0, t1);
+  d = fmaf(t0, 0.00390625f, d);
+  d = fmaf(t1, 0.000244140625f, d);
+  f2_split(aC, t0, t1);
+  da = fmaf(t0 + t1, 1.52587890625e-05f, d);
+  f2_split(bA, t0, t1);
+  d = fmaf(t1, 0.0625f, t0);
+  f2_split(bB, t0, t1);
+  d = fmaf(t0, 0.00390625f, d);
+  d = fmaf(t1, 0.000244140625f, d);
+  f2_split(bC, t0, t1);
+  db = fmaf(t0 + t1, 1.52587890625e-05f, d);
+}
+
+__device__ __forceinline__ float dot_int8(const uint4 c, const f2 (&xp)[8]) {
+  const f2 off2 = f2_make(8388736.0f, 8388736.0f);     // 2^23 + 128
+  f2 a0 = f2_zero(), a1 = f2_zero();
+  const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int wi = 0; wi < 4; wi++) {
+    const uint32_t w = wv[wi] ^ 0x80808080u;
+    f2 q01 = f2_sub(f2_bits(prmt(w, kMagic, 0x7540u), prmt(w, kMagic, 0x7541u)), off2);
+    f2 q23 = f2_sub(f2_bits(prmt(w, kMagic, 0x7542u), prmt(w, kMagic, 0x7543u)), off2);
+    a0 = f2_fma(q01, xp[2 * wi + 0], a0);
+    a1 = f2_fma(q23, xp[2 * wi + 1], a1);
+  }
+  float c0, c1, c2, c3;
+  f2_split(a0, c0, c1);
+  f2_split(a1, c2, c3);
+  return (c0 + c1) + (c2 + c3);
+}
+
+__device__ __forceinline__ float dot_q1(const uint32_t w, const f2 (&xp)[16]) {
+  f2 a[4] = {f2_zero(), f2_zero(), f2_zero(), f2_zero()};
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float xa, xb;
+    f2_split(xp[j / 2], xa, xb);
+    uint32_t sa = xor_andnot(__float_as_uint(xa), w << (31 - j), 0x80000000u);
+    uint32_t sb = xor_andnot(__float_as_uint(xb), w << (30 - j), 0x80000000u);
+    a[(j / 2) & 3] = f2_add(a[(j / 2) & 3], f2_bits(sa, sb));
+  }
+  float t[8];
+  f2_split(a[0], t[0], t[1]);
+  f2_split(a[1], t[2], t[3]);
+  f2_split(a[2], t[4], t[5]);
+  f2_split(a[3], t[6], t[7]);
+  return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+}
+
+// Register pair (0 .. PAIRS-1) and slot (0: .x, 1: .y) of activation j
+// (0 .. W-1) of a lane.
+template <int BITS>
+__device__ __forceinline__ int pair_of(int j, int &slot) {
+  if constexpr (BITS == 4) {
+    // per word: (x0,x1) (x2,x3) (x5,x6) (x4,x7)
+    const int o = j & 7;
+    const int pidx = (o < 4) ? (o >> 1) : (o == 4 || o == 7) ? 3 : 2;
+    slot = (o == 1 || o == 3 || o == 6 || o == 7) ? 1 : 0;
+    return 4 * (j >> 3) + pidx;
+  } else {
+    slot = j & 1;
+    return j >> 1;
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams p) {
+  using L = Lane<BITS>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int S = p.stages;
+  const uint32_t sbase = smem_addr(smem);
+  const int code_stage_bytes = p.stage_rows * p.row_bytes;
+  const uint16_t *sc = reinterpret_cast<const uint16_t *>(smem + p.off_coef);
+  const uint16_t *bi = sc + p.rows_per_cta * p.G;
+  f2 *xs = reinterpret_cast<f2 *>(smem + p.off_x);                 // [segs][PAIRS][32 lanes]
+  float *red = reinterpret_cast<float *>(smem + p.off_red);        // [rows_per_cta][segs]
+  const uint32_t bars = sbase + p.off_bar;
+  auto full = [&](int s) { return bars + 8 * s; };
+  auto empty = [&](int s) { return bars + 8 * (S + s); };
+  const uint32_t coef_full = bars + 8 * (2 * S);
+  const uint32_t done_bar = bars + 8 * (2 * S + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_bar + 8 * (2 * S + 2));
+  const WaitCtl ctl{abort_flag, &g_gemv_status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int consumers = p.segs * p.wps;
+  const int n_begin = blockIdx.x * p.rows_per_cta;
+  const int rows = min(p.N, n_begin + p.rows_per_cta) - n_begin;      // rows of this CTA
+  const int nst = (rows + p.stage_rows - 1) / p.stage_rows;
+  const int groups_per_stage = p.stage_rows / RG;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; s++) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), groups_per_stage * p.segs);   // one arrival per (group, segment)
+    }
+    mbar_init(coef_full, 1);
+    mbar_init(done_bar, consumers);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const uint32_t gbytes = (uint32_t)rows * p.G * 2;
+      mbar_arrive_expect_tx(coef_full, gbytes * (BITS == 4 ? 2 : 1));
+      bulk_load(sbase + p.off_coef, p.scales + (int64_t)n_begin * p.G, gbytes, coef_full, pol);
+      if (BITS == 4)
+        bulk_load(sbase + p.off_coef + p.rows_per_cta * p.G * 2, p.biases + (int64_t)n_begin * p.G, gbytes,
+                  coef_full, pol);
+      int j = 0;
+      bool ok = true;
+      for (; j < nst; j++) {
+        const int s = j % S;
+        const uint32_t ph = (j / S) & 1;
+        if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
+        const int r0 = j * p.stage_rows;
+        const uint32_t cbytes = (uint32_t)min(p.stage_rows, rows - r0) * p.row_bytes;
+        mbar_arrive_expect_tx(full(s), cbytes);
+        bulk_load(sbase + s * code_stage_bytes, p.codes + (int64_t)(n_begin + r0) * p.row_bytes, cbytes, full(s),
+                  pol);
+      }
+      if (!ok) {
+        const int first = j > S ? j - S : 0;
+        for (int i = first; i < j; i++) wait_drain(full(i % S), (i / S) & 1);
+      }
+      wait_drain(coef_full, 0);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int cw = warp - 1;
+  const int ct = cw * 32 + lane;                                // consumer thread index
+  const int nthreads = consumers * 32;
+  pdl_wait();                                                    // x is written by the previous kernel
+  {
+    // x, once per CTA, coalesced; stored as each lane's register pairs
+    const int units = p.K / 4;
+    for (int u = ct; u < units; u += nthreads) {
+      const float4 v = ld_nc_f4(p.x + 4 * u);
+      const int k = 4 * u;
+      const int sg = k / L::SEG_W, l = (k % L::SEG_W) / L::W, j = k % L::W;
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        int slot;
+        const int pi = pair_of<BITS>(j + e, slot);
+        float *dst = reinterpret_cast<float *>(&xs[(sg * L::PAIRS + pi) * 32 + l]);
+        dst[slot] = vv[e];
+      }
+    }
+    // consumer warps only; every consumer thread reaches it (no exit before)
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  }
+  const int seg = cw % p.segs, t0 = cw / p.segs;
+  f2 xp[L::PAIRS];
+#pragma unroll
+  for (int i = 0; i < L::PAIRS; i++) xp[i] = xs[(seg * L::PAIRS + i) * 32 + lane];
+  float xsum = 0.0f;
+  if constexpr (BITS == 4) {
+#pragma unroll
+    for (int i = 0; i < L::PAIRS; i++) {
+      float a, b;
+      f2_split(xp[i], a, b);
+      xsum += a + b;
+    }
+  }
+  const int g = (seg * L::SEG_W + lane * L::W) >> p.gshift;    // a lane chunk lies in one group
+  const int lane_off = seg * L::SEG_BYTES + lane * L::BYTES;
+  bool ok = __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
+
+  const int ngroups = (rows + RG - 1) / RG;
+  for (int grp = t0; ok && grp < ngroups; grp += p.wps) {
+    const int j = grp / groups_per_stage;                        // stage holding this group
+    const int s = j % S;
+    const uint32_t ph = (j / S) & 1;
+    if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
+    const int rbase = grp * RG;                                  // first row (within the CTA)
+    const int nr = min(RG, rows - rbase);
+    const uint8_t *st = smem + s * code_stage_bytes + (rbase - j * p.stage_rows) * p.row_bytes;
+    float part[RG];
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int rr = 0; rr < RG; rr += 2) {
+        const int ra = rr < nr ? rr : 0, rb = rr + 1 < nr ? rr + 1 : 0;
+        float da, db;
+        dot2_int4(*reinterpret_cast<const uint4 *>(st + ra * p.row_bytes + lane_off),
+                  *reinterpret_cast<const uint4 *>(st + rb * p.row_bytes + lane_off), xp, da, db);
+        const int ia = (rbase + ra) * p.G + g, ib = (rbase + rb) * p.G + g;
+        part[rr] = fmaf(h2f(sc[ia]), da, h2f(bi[ia]) * xsum);
+        part[rr + 1] = fmaf(h2f(sc[ib]), db, h2f(bi[ib]) * xsum);
+      }
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < RG; rr++) {
+        const int r = rr < nr ? rr : 0;
+        const uint8_t *cp = st + r * p.row_bytes + lane_off;
+        const float sv = h2f(sc[(rbase + r) * p.G + g]);
+        if constexpr (BITS == 8) {
+          part[rr] = sv * dot_int8(*reinterpret_cast<const uint4 *>(cp), xp);
+        } else {
+          part[rr] = sv * dot_q1(*reinterpret_cast<const uint32_t *>(cp), xp);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));                        // this group's codes are consumed
+    // transposing butterfly: 4 row partials over 32 lanes in 6 shuffles;
+    // afterwards lane l holds the warp total of row 2*bit4(l) + bit3(l)
+    const bool h16 = lane & 16, h8 = lane & 8;
+    float k0 = h16 ? part[2] : part[0], k1 = h16 ? part[3] : part[1];
+    const float s0 = h16 ? part[0] : part[2], s1 = h16 ? part[1] : part[3];
+    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    float k = h8 ? k1 : k0;
+    const float sk = h8 ? k0 : k1;
+    k += __shfl_xor_sync(0xffffffffu, sk, 8);
+    k += __shfl_xor_sync(0xffffffffu, k, 4);
+    k += __shfl_xor_sync(0xffffffffu, k, 2);
+    k += __shfl_xor_sync(0xffffffffu, k, 1);
+    const int rr = (h16 ? 2 : 0) + (h8 ? 1 : 0);
+    if ((lane & 7) == 0 && rr < nr) red[(rbase + rr) * p.segs + seg] = k;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(done_bar);
+  if (!ok) return;
+  // one thread per row adds the segment totals in segment order
+  if (!__all_sync(0xffffffffu, wait_bounded(done_bar, 0, ctl))) return;
+  for (int r = ct; r < rows; r += nthreads) {
+    float acc = 0.0f;
+    for (int q = 0; q < p.segs; q++) acc += red[r * p.segs + q];
+    p.y[n_begin + r] = acc;
+  }
+}
+
+int sm_count_stream() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+template <int BITS>
+bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &threads, size_t &smem) {
+  using L = Lane<BITS>;
+  if (K % L::SEG_W != 0) return false;
+  const int G = (int)(K / group);
+  if ((G * 2) % 16 != 0) return false;                   // coefficient rows must be 16-byte multiples
+  p.N = (int)N;
+  p.K = (int)K;
+  p.G = G;
+  p.gshift = __builtin_ctz((unsigned)group);
+  p.row_bytes = (int)(K * BITS / 8);
+  p.segs = (int)(K / L::SEG_W);
+  if (p.segs > kMaxConsumerWarps) return false;
+  grid = (int)((N + RG - 1) / RG);
+  if (grid > sm_count_stream()) grid = sm_count_stream();
+  p.rows_per_cta = (int)((N + grid - 1) / grid);
+  grid = (int)((N + p.rows_per_cta - 1) / p.rows_per_cta);
+  p.stage_rows = STAGE_ROWS_MAX;
+  while (p.stage_rows > RG && p.stage_rows / 2 >= p.rows_per_cta) p.stage_rows /= 2;
+  const int nst = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
+  const int coef = p.rows_per_cta * G * 2 * (BITS == 4 ? 2 : 1);
+  const int xbytes = (int)K * 4;
+  const int redb = p.rows_per_cta * p.segs * 4;
+  const int fixed = coef + xbytes + redb + 8 * 64;
+  const int stage_bytes = p.stage_rows * p.row_bytes;
+  int S = (kSmemBudget - fixed) / stage_bytes;
+  if (S > nst) S = nst;
+  if (S < 1) return false;
+  p.stages = S;
+  p.off_coef = S * stage_bytes;
+  p.off_x = (p.off_coef + coef + 15) & ~15;
+  p.off_red = p.off_x + xbytes;
+  p.off_bar = (p.off_red + redb + 7) & ~7;
+  smem = (size_t)p.off_bar + 8 * (2 * S + 2) + 16;
+  int wps = kMaxConsumerWarps / p.segs;
+  const int ngroups = (p.rows_per_cta + RG - 1) / RG;
+  if (wps > ngroups) wps = ngroups;
+  if (wps < 1) wps = 1;
+  p.wps = wps;
+  threads = 32 * (1 + p.segs * wps);
+  return true;
+}
+
+template <int BITS>
+cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t smem, cudaStream_t s) {
+  auto kern = gemv_stream_kernel<BITS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // Every instantiation asks for the same (largest) shared-memory carveout, so
+  // that a CTA of the next decode product can join an SM that still runs one
+  // of the previous product (programmatic dependent launch overlap).
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p0);
+}
+
+}  // namespace
+
+// Returns cudaErrorNotSupported when the shape does not fit this kernel's
+// layout (K not a whole number of warp segments, more than 15 segments,
+// coefficient rows not 16-byte multiples, or a slab too large for shared
+// memory); the caller then uses the register-fed kernel.
+cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint16_t *scales,
+                               const uint16_t *biases, float *y, int64_t N, int64_t K, int bits, int group,
+                               cudaStream_t s) {
+  StreamParams p{};
+  p.x = x;
+  p.codes = reinterpret_cast<const uint8_t *>(codes);
+  p.scales = scales;
+  p.biases = biases;
+  p.y = y;
+  int grid = 0, threads = 0;
+  size_t smem = 0;
+  bool ok = bits == 4 ? plan<4>(N, K, group, p, grid, threads, smem)
+            : bits == 8 ? plan<8>(N, K, group, p, grid, threads, smem)
+                        : plan<1>(N, K, group, p, grid, threads, smem);
+  if (!ok) return cudaErrorNotSupported;
+  if (bits == 4) return launch_stream<4>(p, grid, threads, smem, s);
+  if (bits == 8) return launch_stream<8>(p, grid, threads, smem, s);
+  return launch_stream<1>(p, grid, threads, smem, s);
+}
+
+cudaError_t read_clear_gemv_status(int *status, cudaStream_t s) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_gemv_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_gemv_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+  }
+  *status = v;
+  return cudaSuccess;
+}
+
+}  // namespace qmm

@@ -151,3 +151,27 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 
 }  // namespace sm100
 }  // namespace qmm
+
+namespace qmm {
+namespace sm100 {
+
+// L2 policy for data read exactly once (weights in a decode pass).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Non-tensor bulk copy global -> shared (TMA engine); `bytes` and both
+// addresses must be multiples of 16.  Completion is signalled as transaction
+// bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+}  // namespace sm100
+}  // namespace qmm

@@ -48,10 +48,12 @@ def run_case(qmm, oracle_mod, M, N, K, bits, group, seed):
 
 
 # small shapes spanning several K-tiles, ragged K tails and ragged row blocks
+# (K a whole number of 1024-weight segments, 512 for INT8, takes the streaming
+# kernel at M = 1; the other K values take the register-fed kernel)
 SMALL = [
-    (4, 64, [128, 1088, 4160]), (4, 32, [96, 2080]), (4, 128, [1152]),
-    (8, 64, [128, 1088, 4160]), (8, 32, [544]), (8, 128, [2176]),
-    (1, 128, [128, 2176, 5120]), (1, 64, [1152]), (1, 32, [384]),
+    (4, 64, [128, 1088, 3072]), (4, 32, [96, 2080]), (4, 128, [1152, 2048]),
+    (8, 64, [128, 1088, 2048]), (8, 32, [544, 1024]), (8, 128, [2176]),
+    (1, 128, [128, 2176, 5120]), (1, 64, [1152, 2048]), (1, 32, [384]),
 ]
 
 
