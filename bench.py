@@ -43,8 +43,8 @@ HEADLINE_DOWN = "decode_int4_down_k6144_n2048"
 WORKLOAD_NAME = "decode_int4_g64_mlp_up_k2048_n6144+down_k6144_n2048"
 METRIC = "decode qGEMV weight-GB/s (% of HBM peak)"
 NOMINAL_HBM_GBS = 8000.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_int4_decode_mlp.md")
-GEMV_SOURCE = os.path.join(ROOT, "quantized_weight_gb300", "csrc", "gemv.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_stream_int4_decode_mlp.md")
+GEMV_SOURCE = os.path.join(ROOT, "quantized_weight_gb300", "csrc", "gemv_stream.cu")
 
 
 # ---------------------------------------------------------------- algorithmic work
@@ -324,6 +324,21 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def profile_workload(name, launches):
+    """Plain launches of one workload on the current stream, nothing timed."""
+    import torch
+    from quantized_weight_gb300 import build as qbuild
+    from quantized_weight_gb300 import qmm
+    qbuild.build()
+    w, d, t = device_inputs(name, 0, torch, qmm)
+    y = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    f = (gemm_call if w.prefill else gemv_call)(qmm, t, w, y)
+    for _ in range(launches):
+        f()
+    qmm.check()
+    print(json.dumps({"profiled": name, "launches": launches}), flush=True)
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -337,6 +352,9 @@ def main():
     ap.add_argument("--no-clock-load", action="store_true",
                     help="skip the 1 s sustained replay after the timed region (for profiler runs)")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--profile-workload", default=None,
+                    help="only run LAUNCHES plain launches of one named workload (for profiler captures)")
+    ap.add_argument("--launches", type=int, default=5)
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -345,6 +363,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.profile_workload:
+        return profile_workload(args.profile_workload, args.launches)
 
     import torch
     import torch.distributed as dist
@@ -479,7 +499,7 @@ def main():
         "parity": {"sampled_rel_l2_vs_oracle": parity, "tolerance": 1e-5},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic_from_profile(),
-                     "kernel": "gemv_kernel<4,1,8,2,4> (INT4 decode product)",
+                     "kernel": "gemv_stream_kernel<4> (INT4 decode product)",
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,

@@ -15,6 +15,7 @@ namespace qmm {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: every legitimate wait is far shorter
 constexpr int kTimeoutStatus = -6;                 // QMM_ERR_DEVICE_TIMEOUT
+constexpr uint32_t kSleepNs = 200000;              // longest sleep inside one try_wait
 
 struct WaitCtl {
   volatile int *abort;   // shared memory, CTA-wide
@@ -23,18 +24,18 @@ struct WaitCtl {
 
 // True once the phase with `parity` completed; false if this CTA aborted or
 // the wait ran out of time (which then aborts the CTA and records the status).
+// A waiting thread sleeps inside try_wait (woken when the phase completes), so
+// waiting warps take no issue slots from the warps doing work.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl &c) {
   if (sm100::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = sm100::globaltimer_ns();
-  for (uint32_t it = 1;; it++) {
-    if (sm100::mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*c.abort) return false;
-      if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) {
-        *c.abort = 1;
-        atomicExch(c.status, kTimeoutStatus);
-        return false;
-      }
+  for (;;) {
+    if (sm100::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    if (*c.abort) return false;
+    if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *c.abort = 1;
+      atomicExch(c.status, kTimeoutStatus);
+      return false;
     }
   }
 }
@@ -42,7 +43,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 // Used only while draining after an abort: bounded, records nothing.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = sm100::globaltimer_ns();
-  while (!sm100::mbar_try_wait(bar, parity))
+  while (!sm100::mbar_try_wait_sleep(bar, parity, kSleepNs))
     if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) break;
 }
 

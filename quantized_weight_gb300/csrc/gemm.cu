@@ -1,33 +1,37 @@
 // gemm.cu -- the prefill product y[M, N] = x[M, K] * dequant(W)^T on tcgen05.
 //
-// The page of the "... Tesla C2075 ..." paper (section 3.1 "Prefill projections:
-// dequantize, then call the vendor") dequantizes every 8-bit weight into an FP32
-// scratch matrix and then calls the vendor GEMM; the Maxwell Q1 page ("A 27B
-// model on two 4GB Maxwell GPUs", section "A packed Q1 prefill kernel with a
-// narrow dispatch window") expands Q1 weights to FP32 before SGEMM.  Here the
+// The "... Tesla C2075 ..." paper (section 3.1 "Prefill projections: dequantize,
+// then call the vendor") dequantizes every 8-bit weight into an FP32 scratch
+// matrix and then calls the vendor GEMM; the Maxwell Q1 page ("A 27B model on
+// two 4GB Maxwell GPUs", section "A packed Q1 prefill kernel with a narrow
+// dispatch window") expands Q1 weights to FP32 before SGEMM.  Here the
 // dequantization is fused into the tensor-core pipeline instead: codes travel
-// from HBM to shared memory by TMA, four warps turn each 128-row x 64-k code
+// from HBM to shared memory by TMA, eight warps turn each 128-row x 64-k code
 // tile into bf16 directly in the 128-byte-swizzled K-major layout the tensor
 // core reads, and no dequantized weight ever reaches global memory.
 //
-// Roles of one persistent CTA per SM (10 warps):
+// Roles of one persistent CTA per SM (14 warps):
 //   warp 0      TMA producer: per K-step, the x tile (bf16, BN tokens x 64 k,
 //               128-byte swizzle) and the code tile (128 rows x 32 bytes)
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warps 2-5   dequantization: thread t owns weight row t of the tile:
-//               w = s*q + b in float32 (exact products, one rounding), then
-//               round-to-nearest-even bf16, stored swizzled, proxy-fenced
-//   warps 6-9   epilogue: tcgen05.ld of the f32 accumulator, y stored with
+//   warps 2-9   dequantization, two threads per weight row (32 k each):
+//               w = s*q + b in float32 (exact product, one rounding), then
+//               round-to-nearest-even bf16, stored swizzled, proxy-fenced;
+//               the row's scales and biases come eight groups at a time
+//               with 16-byte loads, one chunk ahead
+//   warps 10-13 epilogue: tcgen05.ld of the f32 accumulator, y stored with
 //               32 consecutive n per warp-wide store
 //
 // The MMA computes D[128 weight rows, BN tokens] = A * B^T with A = the
 // dequantized weight tile and B = the x tile, i.e. the transpose of a y tile;
 // putting the weights on the M side lets one dequantized tile serve BN tokens.
-// Two accumulators of BN columns live in TMEM so the epilogue of one tile
-// overlaps the main loop of the next.  Stage buffers are guarded by mbarriers
-// (TMA -> full, dequant -> afull, MMA commit -> empty).
+// BN (a multiple of 16, at most 256) is chosen per call so that the tiles
+// fill whole waves of the SMs.  Two accumulators of 256 columns live in TMEM
+// so the epilogue of one tile overlaps the main loop of the next.  Stage
+// buffers are guarded by mbarriers (TMA -> full, dequant -> afull,
+// MMA commit -> empty).
 //
-// Every wait is bounded by wall time (globaltimer).  A wait that runs out
+// Every wait is bounded by wall time (bounded_wait.cuh).  A wait that runs out
 // records QMM_ERR_DEVICE_TIMEOUT in a device status word, raises a CTA-wide
 // abort flag that the other roles poll, drains this CTA's outstanding TMA
 // copies and MMAs (again with bounded waits), frees TMEM and returns.
@@ -49,23 +53,23 @@ using namespace sm100;
 
 constexpr int BM = 128;                // weight rows per tile (MMA M)
 constexpr int BK = 64;                 // k per stage: one 128-byte swizzle atom of bf16
+constexpr int BN_MAX = 256;            // tokens per tile (MMA N), at most
 constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
-constexpr int NUM_THREADS = 320;
-constexpr int DQ_WARP0 = 2, EPI_WARP0 = 6;
+constexpr int DQ_WARP0 = 2, DQ_WARPS = 8, EPI_WARP0 = DQ_WARP0 + DQ_WARPS;
+constexpr int NUM_THREADS = 32 * (EPI_WARP0 + 4);
+constexpr int DQ_THREADS = 32 * DQ_WARPS;
 
-template <int BN>
 struct Smem {
-  static constexpr int A_BYTES = BM * BK * 2;      // 16 KB dequantized weights (bf16)
-  static constexpr int B_BYTES = BN * BK * 2;      // x tile (bf16)
-  static constexpr int C_BYTES = BM * BK / 2;      // 4 KB codes
+  static constexpr int A_BYTES = BM * BK * 2;        // 16 KB dequantized weights (bf16)
+  static constexpr int B_BYTES = BN_MAX * BK * 2;    // 32 KB x tile (bf16), BN rows used
+  static constexpr int C_BYTES = BM * BK / 2;        // 4 KB codes
   static constexpr int STAGE = A_BYTES + B_BYTES + C_BYTES;
-  static constexpr int BAR_OFF = STAGES * STAGE;   // multiple of 1024
-  static constexpr int BARS = 3 * STAGES + 4 + 1;  // full, afull, empty, acc_full[2], acc_empty[2], drain
+  static constexpr int BAR_OFF = STAGES * STAGE;     // multiple of 1024
+  static constexpr int BARS = 3 * STAGES + 4 + 1;    // full, afull, empty, acc_full[2], acc_empty[2], drain
   static constexpr int TOTAL = BAR_OFF + BARS * 8 + 16 /* tmem slot + abort flag */;
-  static constexpr int ALLOC = TOTAL + 1024;       // slack to align the base to 1024
-  static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                        : (2 * BN <= 256) ? 256 : 512;
+  static constexpr int ALLOC = TOTAL + 1024;         // slack to align the base to 1024
+  static constexpr uint32_t TMEM_COLS = 2 * BN_MAX;  // two accumulators
 };
 
 struct GemmParams {
@@ -75,6 +79,8 @@ struct GemmParams {
   int M, N, K;
   int gshift;
   int groups_per_row;
+  int coef_vec;          // coefficient rows load as 16-byte vectors
+  int bn;
   int m_blocks, n_blocks, tiles;
 };
 
@@ -119,11 +125,16 @@ __device__ __forceinline__ void scale_pairs(float s, f2 (&sp)[4]) {
   sp[3] = f2_make(s3, s4);
 }
 
-template <int BN>
+// Half i (0..7) of eight binary16 values held in a uint4.
+__device__ __forceinline__ uint16_t half_at(const uint4 v, int i) {
+  const uint32_t w = (i & 4) ? ((i & 2) ? v.w : v.z) : ((i & 2) ? v.y : v.x);
+  return (uint16_t)((i & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     qmm_gemm_int4_kernel(const __grid_constant__ CUtensorMap tmap_x,
                          const __grid_constant__ CUtensorMap tmap_codes, const GemmParams p) {
-  using S = Smem<BN>;
+  using S = Smem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // align the working area to 1024 bytes (128-byte swizzle atoms)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -146,11 +157,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ksteps = p.K / BK;
+  const int bn = p.bn;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; s++) {
       mbar_init(full(s), 1);
-      mbar_init(afull(s), 128);
+      mbar_init(afull(s), DQ_THREADS);
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; b++) {
@@ -172,6 +184,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmap_x);
       tma_prefetch_desc(&tmap_codes);
+      const uint32_t tx = (uint32_t)bn * BK * 2 + S::C_BYTES;
       int it = 0;                   // global K-step counter of this CTA
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
@@ -180,8 +193,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
-          mbar_arrive_expect_tx(full(s), S::B_BYTES + S::C_BYTES);
-          tma_load_2d(b_buf(s), &tmap_x, kb * BK, mb * BN, full(s));
+          mbar_arrive_expect_tx(full(s), tx);
+          tma_load_2d(b_buf(s), &tmap_x, kb * BK, mb * bn, full(s));
           tma_load_2d(c_buf(s), &tmap_codes, kb * (BK / 2), nb * BM, full(s));
         }
       }
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      const uint32_t idesc = idesc_bf16_f32(BM, bn);
       int it = 0, local = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, local++) {
@@ -202,7 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t use = (local >> 1) & 1;
         if (!wait_bounded(acc_empty(buf), use ^ 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * BN;
+        const uint32_t d_tmem = tmem_base + buf * BN_MAX;
         for (int kb = 0; kb < ksteps; kb++, it++) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -227,52 +240,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp < EPI_WARP0) {
     // ------------------------------------------------------------ dequantization
-    const int t = threadIdx.x - DQ_WARP0 * 32;      // weight row within the tile
+    const int t = threadIdx.x - DQ_WARP0 * 32;      // 0 .. 255
+    const int r = t >> 1, half = t & 1;             // weight row within the tile, k half
+    const int G = p.groups_per_row;
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const int nb = tile / p.m_blocks;
-      const int row = nb * BM + t;
+      const int row = nb * BM + r;
       const bool row_ok = row < p.N;
-      const uint16_t *srow = p.scales + (int64_t)(row_ok ? row : 0) * p.groups_per_row;
-      const uint16_t *brow = p.biases + (int64_t)(row_ok ? row : 0) * p.groups_per_row;
-      // coefficients of K-steps kb, kb+1, kb+2 in flight (rotating registers)
-      uint16_t s0 = 0, b0 = 0, s1 = 0, b1 = 0, s2 = 0, b2v = 0;
-      if (row_ok) {
-        s0 = ld_nc_u16(srow + ((0 * BK) >> p.gshift));
-        b0 = ld_nc_u16(brow + ((0 * BK) >> p.gshift));
-        if (ksteps > 1) { s1 = ld_nc_u16(srow + ((1 * BK) >> p.gshift)); b1 = ld_nc_u16(brow + ((1 * BK) >> p.gshift)); }
-        if (ksteps > 2) { s2 = ld_nc_u16(srow + ((2 * BK) >> p.gshift)); b2v = ld_nc_u16(brow + ((2 * BK) >> p.gshift)); }
+      const uint16_t *srow = p.scales + (int64_t)(row_ok ? row : 0) * G;
+      const uint16_t *brow = p.biases + (int64_t)(row_ok ? row : 0) * G;
+      // coefficients: eight groups per 16-byte load, current and next chunk
+      uint4 sc_cur = make_uint4(0, 0, 0, 0), bc_cur = sc_cur, sc_nxt = sc_cur, bc_nxt = sc_cur;
+      int cur_chunk = 0;
+      if (p.coef_vec && row_ok) {
+        sc_cur = ld_stream_u4(srow);
+        bc_cur = ld_stream_u4(brow);
+        if (G > 8) {
+          sc_nxt = ld_stream_u4(srow + 8);
+          bc_nxt = ld_stream_u4(brow + 8);
+        }
       }
       for (int kb = 0; kb < ksteps; kb++, it++) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        uint16_t s3 = 0, b3 = 0;
-        if (row_ok && kb + 3 < ksteps) {
-          s3 = ld_nc_u16(srow + (((kb + 3) * BK) >> p.gshift));
-          b3 = ld_nc_u16(brow + (((kb + 3) * BK) >> p.gshift));
+        const int g = (kb * BK) >> p.gshift;
+        uint16_t sb = 0, bb = 0;
+        if (row_ok) {
+          if (p.coef_vec) {
+            if ((g >> 3) != cur_chunk) {
+              cur_chunk = g >> 3;
+              sc_cur = sc_nxt;
+              bc_cur = bc_nxt;
+              if ((cur_chunk + 1) * 8 < G) {
+                sc_nxt = ld_stream_u4(srow + (cur_chunk + 1) * 8);
+                bc_nxt = ld_stream_u4(brow + (cur_chunk + 1) * 8);
+              }
+            }
+            sb = half_at(sc_cur, g & 7);
+            bb = half_at(bc_cur, g & 7);
+          } else {
+            sb = ld_nc_u16(srow + g);
+            bb = ld_nc_u16(brow + g);
+          }
         }
-        const float sf = row_ok ? h2f(s0) : 0.0f;
-        const float bf = row_ok ? h2f(b0) : 0.0f;
-        if (!wait_bounded(full(s), ph, ctl)) { ok = false; break; }
-        const uint4 *cw = reinterpret_cast<const uint4 *>(c_ptr(s) + t * 32);
-        const uint4 lo = cw[0], hi = cw[1];
+        const float sf = row_ok ? h2f(sb) : 0.0f;
+        const float bf = row_ok ? h2f(bb) : 0.0f;
         f2 sp[4];
         scale_pairs(sf, sp);
-        const f2 bb = f2_make(bf, bf);
-        const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        const uint32_t arow = a_buf(s) + t * 128;
+        const f2 b2 = f2_make(bf, bf);
+        if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
+        const uint4 cw = *reinterpret_cast<const uint4 *>(c_ptr(s) + t * 16);   // 32 codes of row r
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        const uint32_t arow = a_buf(s) + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
-          const uint4 v = dequant_word_bf16(words[c], sp, bb);
-          const uint32_t dst = arow + ((c ^ (t & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
-                       "r"(v.z), "r"(v.w)
+        for (int i = 0; i < 4; i++) {
+          const int c = 4 * half + i;                                      // 16-byte chunk: k = 8c..8c+7
+          const uint4 v = dequant_word_bf16(words[i], sp, b2);
+          const uint32_t dst = arow + ((c ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
+                       "r"(v.w)
                        : "memory");
         }
         fence_proxy_async_smem();
         mbar_arrive(afull(s));
-        s0 = s1; b0 = b1; s1 = s2; b1 = b2v; s2 = s3; b2v = b3;
       }
     }
   } else {
@@ -285,20 +317,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int mb = tile % p.m_blocks, nb = tile / p.m_blocks;
       const int buf = local & 1;
       const uint32_t use = (local >> 1) & 1;
-      if (!wait_bounded(acc_full(buf), use, ctl)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait_bounded(acc_full(buf), use, ctl))) { ok = false; break; }
       tc_fence_after();
       const int n = nb * BM + r;
-      const int m0 = mb * BN;
+      const int m0 = mb * bn;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN_MAX;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + c0, v);
-        tmem_ld_wait();
-        if (n < p.N) {
+      for (int c0 = 0; c0 < bn; c0 += 32) {
+        if (c0 + 32 <= bn) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c0, v);
+          tmem_ld_wait();
+          if (n < p.N) {
 #pragma unroll
-          for (int j = 0; j < 32; j++) {
-            const int m = m0 + c0 + j;
-            if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
+            for (int j = 0; j < 32; j++) {
+              const int m = m0 + c0 + j;
+              if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
+            }
+          }
+        } else {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tbase + c0, v);
+          tmem_ld_wait();
+          if (n < p.N) {
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+              const int m = m0 + c0 + j;
+              if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
+            }
           }
         }
       }
@@ -341,43 +387,26 @@ int sm_count_gemm() {
   return n;
 }
 
-template <int BN>
-cudaError_t launch_bn(const uint16_t *x_bf16, const uint32_t *codes, const GemmParams &p0,
-                      cudaStream_t s) {
-  using S = Smem<BN>;
-  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
-  if (!encode) return cudaErrorNotSupported;
-  CUtensorMap tx, tc;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)p0.K, (cuuint64_t)p0.M};
-    cuuint64_t strides[1] = {(cuuint64_t)p0.K * 2};
-    cuuint32_t box[2] = {BK, BN};
-    cuuint32_t es[2] = {1, 1};
-    if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x_bf16), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+// Token-tile width: the multiple of 16 (<= 256) that minimizes
+// waves * max(BN, floor), where a wave is one tile per SM and `floor` stands
+// for the per-K-step dequantization time below which a narrower tile does not
+// get faster.  Ties go to the wider tile.
+int pick_bn(int64_t M, int64_t N, int sms) {
+  const int64_t nblk = (N + BM - 1) / BM;
+  const int64_t floor_bn = 128;
+  int best = 16;
+  int64_t best_cost = -1;
+  for (int bn = 16; bn <= BN_MAX; bn += 16) {
+    const int64_t tiles = ((M + bn - 1) / bn) * nblk;
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const int64_t cost = waves * (bn > floor_bn ? bn : floor_bn);
+    if (best_cost < 0 || cost <= best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+    if (bn >= M) break;            // wider tiles only add padding
   }
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)p0.K / 2, (cuuint64_t)p0.N};
-    cuuint64_t strides[1] = {(cuuint64_t)p0.K / 2};
-    cuuint32_t box[2] = {BK / 2, BM};
-    cuuint32_t es[2] = {1, 1};
-    if (encode(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(codes), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  GemmParams p = p0;
-  p.m_blocks = (p.M + BN - 1) / BN;
-  p.n_blocks = (p.N + BM - 1) / BM;
-  p.tiles = p.m_blocks * p.n_blocks;
-  auto kern = qmm_gemm_int4_kernel<BN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
-  if (e != cudaSuccess) return e;
-  const int grid = p.tiles < sm_count_gemm() ? p.tiles : sm_count_gemm();
-  kern<<<grid, NUM_THREADS, S::ALLOC, s>>>(tx, tc, p);
-  return cudaGetLastError();
+  return best;
 }
 
 }  // namespace
@@ -385,6 +414,7 @@ cudaError_t launch_bn(const uint16_t *x_bf16, const uint32_t *codes, const GemmP
 cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
                         const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int group,
                         cudaStream_t s) {
+  using S = Smem;
   GemmParams p{};
   p.scales = scales;
   p.biases = biases;
@@ -394,9 +424,41 @@ cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uin
   p.K = (int)K;
   p.gshift = __builtin_ctz((unsigned)group);
   p.groups_per_row = (int)(K / group);
-  if (M > 128) return launch_bn<256>(x_bf16, codes, p, s);
-  if (M > 64) return launch_bn<128>(x_bf16, codes, p, s);
-  return launch_bn<64>(x_bf16, codes, p, s);
+  p.coef_vec = (p.groups_per_row % 8 == 0) ? 1 : 0;   // rows are then 16-byte multiples (bases are 16-aligned)
+  p.bn = pick_bn(M, N, sm_count_gemm());
+  p.m_blocks = (int)((M + p.bn - 1) / p.bn);
+  p.n_blocks = (int)((N + BM - 1) / BM);
+  p.tiles = p.m_blocks * p.n_blocks;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tx, tc;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {BK, (cuuint32_t)p.bn};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x_bf16), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+    cuuint32_t box[2] = {BK / 2, BM};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(codes), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  auto kern = qmm_gemm_int4_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+  if (e != cudaSuccess) return e;
+  const int grid = p.tiles < sm_count_gemm() ? p.tiles : sm_count_gemm();
+  kern<<<grid, NUM_THREADS, S::ALLOC, s>>>(tx, tc, p);
+  return cudaGetLastError();
 }
 
 cudaError_t read_clear_gemm_status(int *status, cudaStream_t s) {

@@ -191,8 +191,11 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int consumers = p.segs * p.wps;
-  const int n_begin = blockIdx.x * p.rows_per_cta;
-  const int rows = min(p.N, n_begin + p.rows_per_cta) - n_begin;      // rows of this CTA
+  // rows split evenly over the grid (one CTA per SM): every SM gets the
+  // same work, and under programmatic dependent launch every SM has room for
+  // exactly one CTA of the next product
+  const int n_begin = (int)((int64_t)blockIdx.x * p.N / gridDim.x);
+  const int rows = (int)((int64_t)(blockIdx.x + 1) * p.N / gridDim.x) - n_begin;   // <= rows_per_cta
   const int nst = (rows + p.stage_rows - 1) / p.stage_rows;
   const int groups_per_stage = p.stage_rows / RG;
 
@@ -371,8 +374,7 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   if (p.segs > kMaxConsumerWarps) return false;
   grid = (int)((N + RG - 1) / RG);
   if (grid > sm_count_stream()) grid = sm_count_stream();
-  p.rows_per_cta = (int)((N + grid - 1) / grid);
-  grid = (int)((N + p.rows_per_cta - 1) / p.rows_per_cta);
+  p.rows_per_cta = (int)((N + grid - 1) / grid);            // the largest slab of the even split
   p.stage_rows = STAGE_ROWS_MAX;
   while (p.stage_rows > RG && p.stage_rows / 2 >= p.rows_per_cta) p.stage_rows /= 2;
   const int nst = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
