@@ -261,6 +261,27 @@ def traffic_from_profile():
     return float(m.group(1))
 
 
+# ---------------------------------------------------------------- multi-rank host logic
+
+def slowest_rank_seconds(sec, world, device):
+    """The timed region's length on the slowest rank (every rank gets it).
+    One rank per GPU, each timing its own replica of the workload; the job
+    finishes when the slowest one does."""
+    if world <= 1:
+        return sec
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([sec], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_step, steps, world, sec):
+    """Whole-job weight-GB/s: the bytes all ranks processed over the slowest
+    rank's time (weak scaling: every rank runs the same per-GPU workload)."""
+    return bytes_per_step * steps * world / sec / 1e9
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample(seconds, nthreads=None):
@@ -432,12 +453,9 @@ def main():
         stream.synchronize()
     clocks = sampler.stop()
 
-    if world > 1:
-        tt = torch.tensor([sec], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        sec = float(tt.item())
+    sec = slowest_rank_seconds(sec, world, "cuda")
     ms_per_step = sec / args.steps * 1e3
-    value = step_bytes * args.steps * world / sec / 1e9
+    value = job_gbs(step_bytes, args.steps, world, sec)
     per_launch_s = sec / args.steps / launches_per_step
     achieved = (step_bytes / launches_per_step) / per_launch_s / 1e9
 
@@ -471,8 +489,8 @@ def main():
         f1.record(stream)
         f1.synchronize()
         barrier()
-    e2e_sec = f0.elapsed_time(f1) / 1000.0
-    e2e_val = step_bytes * e2e_steps * world / e2e_sec / 1e9
+    e2e_sec = slowest_rank_seconds(f0.elapsed_time(f1) / 1000.0, world, "cuda")
+    e2e_val = job_gbs(step_bytes, e2e_steps, world, e2e_sec)
 
     del chain
     torch.cuda.empty_cache()
