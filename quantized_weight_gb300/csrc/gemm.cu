@@ -59,6 +59,10 @@ constexpr int UMMA_K = 16;
 constexpr int DQ_WARP0 = 2, DQ_WARPS = 8, EPI_WARP0 = DQ_WARP0 + DQ_WARPS;
 constexpr int NUM_THREADS = 32 * (EPI_WARP0 + 4);
 constexpr int DQ_THREADS = 32 * DQ_WARPS;
+constexpr int DQ_TPR = DQ_THREADS / BM;            // dequantization threads per weight row
+constexpr int DQ_WORDS = (BK / 8) / DQ_TPR;        // 32-bit code words per thread per K-step
+static_assert(DQ_TPR * BM == DQ_THREADS && DQ_WORDS * DQ_TPR * 8 == BK && (DQ_WORDS == 4 || DQ_WORDS == 2),
+              "dequantization split");
 
 struct Smem {
   static constexpr int A_BYTES = BM * BK * 2;        // 16 KB dequantized weights (bf16)
@@ -210,6 +214,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t idesc = idesc_bf16_f32(BM, bn);
       int it = 0, local = 0;
       bool ok = true;
+      // Readiness of stage `it` tested while the previous stage's MMAs were
+      // being issued, so the ~180-cycle latency of the test is hidden; only a
+      // stage found not ready takes the blocking (bounded) wait.
+      bool ready = false;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, local++) {
         const int buf = local & 1;
         const uint32_t use = (local >> 1) & 1;
@@ -219,8 +227,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kb = 0; kb < ksteps; kb++, it++) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!wait_bounded(full(s), ph, ctl) || !wait_bounded(afull(s), ph, ctl)) { ok = false; break; }
+          if (!ready) {
+            const bool f = mbar_test(full(s), ph), a = mbar_test(afull(s), ph);
+            if (!(f || wait_bounded(full(s), ph, ctl)) || !(a || wait_bounded(afull(s), ph, ctl))) {
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
+          const int sn = (it + 1) % STAGES;
+          const uint32_t phn = ((it + 1) / STAGES) & 1;
+          const bool fn = mbar_test(full(sn), phn), an = mbar_test(afull(sn), phn);
           const uint64_t ad = smem_desc_sw128(a_buf(s));
           const uint64_t bd = smem_desc_sw128(b_buf(s));
 #pragma unroll
@@ -229,6 +246,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
           }
           umma_commit(empty(s));          // stage free once these MMAs have read it
+          ready = fn && an;
         }
         if (!ok) break;
         umma_commit(acc_full(buf));       // accumulator complete
@@ -240,11 +258,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp < EPI_WARP0) {
     // ------------------------------------------------------------ dequantization
-    const int t = threadIdx.x - DQ_WARP0 * 32;      // 0 .. 255
-    const int r = t >> 1, half = t & 1;             // weight row within the tile, k half
+    const int t = threadIdx.x - DQ_WARP0 * 32;      // 0 .. DQ_THREADS - 1
+    const int r = t / DQ_TPR, part = t % DQ_TPR;    // weight row within the tile, k part
     const int G = p.groups_per_row;
     int it = 0;
     bool ok = true;
+    bool ready = false;       // stage `it` seen complete by a test issued one K-step early
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const int nb = tile / p.m_blocks;
       const int row = nb * BM + r;
@@ -290,13 +309,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         f2 sp[4];
         scale_pairs(sf, sp);
         const f2 b2 = f2_make(bf, bf);
-        if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
-        const uint4 cw = *reinterpret_cast<const uint4 *>(c_ptr(s) + t * 16);   // 32 codes of row r
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        if (!ready && !__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
+        uint32_t words[DQ_WORDS];                                          // 8 * DQ_WORDS codes of row r
+        if constexpr (DQ_WORDS == 4) {
+          const uint4 cw = *reinterpret_cast<const uint4 *>(c_ptr(s) + t * 16);
+          words[0] = cw.x, words[1] = cw.y, words[2] = cw.z, words[3] = cw.w;
+        } else {
+          const uint2 cw = *reinterpret_cast<const uint2 *>(c_ptr(s) + t * 8);
+          words[0] = cw.x, words[1] = cw.y;
+        }
+        const bool next_ready = mbar_test(full((it + 1) % STAGES), ((it + 1) / STAGES) & 1);
         const uint32_t arow = a_buf(s) + r * 128;
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-          const int c = 4 * half + i;                                      // 16-byte chunk: k = 8c..8c+7
+        for (int i = 0; i < DQ_WORDS; i++) {
+          const int c = DQ_WORDS * part + i;                               // 16-byte chunk: k = 8c..8c+7
           const uint4 v = dequant_word_bf16(words[i], sp, b2);
           const uint32_t dst = arow + ((c ^ (r & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -305,6 +331,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(afull(s));
+        ready = __all_sync(0xffffffffu, next_ready);
       }
     }
   } else {

@@ -40,6 +40,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of the same condition.  A test (or try_wait) takes about
+// 180 cycles to return even when the phase completed long ago, so a thread
+// that knows which phase it needs next issues the test early and reads the
+// result after other work.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // As mbar_try_wait, but the thread may sleep (without issuing) for up to
 // `sleep_ns` while the phase is incomplete; it wakes when the phase completes.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t sleep_ns) {
