@@ -111,11 +111,12 @@ int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scal
 
 int qmm_check(qmm_stream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return QMM_ERR_CUDA;
-  int gemm_status = 0, gemv_status = 0, q1_status = 0;
-  if (qmm::read_clear_gemm_status(&gemm_status, stream) != cudaSuccess) return QMM_ERR_CUDA;
-  if (qmm::read_clear_gemv_status(&gemv_status, stream) != cudaSuccess) return QMM_ERR_CUDA;
-  if (qmm::read_clear_q1_status(&q1_status, stream) != cudaSuccess) return QMM_ERR_CUDA;
-  return (gemm_status != 0 || gemv_status != 0 || q1_status != 0) ? QMM_ERR_DEVICE_TIMEOUT : QMM_OK;
+  int st[4] = {0, 0, 0, 0};
+  if (qmm::read_clear_gemm_status(&st[0], stream) != cudaSuccess) return QMM_ERR_CUDA;
+  if (qmm::read_clear_gemv_status(&st[1], stream) != cudaSuccess) return QMM_ERR_CUDA;
+  if (qmm::read_clear_q1_status(&st[2], stream) != cudaSuccess) return QMM_ERR_CUDA;
+  if (qmm::read_clear_batch_status(&st[3], stream) != cudaSuccess) return QMM_ERR_CUDA;
+  return (st[0] | st[1] | st[2] | st[3]) != 0 ? QMM_ERR_DEVICE_TIMEOUT : QMM_OK;
 }
 
 }  // extern "C"

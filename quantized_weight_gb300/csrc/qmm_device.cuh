@@ -72,6 +72,11 @@ __device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
   return r;
 }
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
 // a * b + c, one rounding per lane
 __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
   f2 r;

@@ -32,6 +32,13 @@ cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint
 cudaError_t launch_gemv_q1(const float *x, const uint32_t *codes, const uint16_t *scales, float *y, int64_t N,
                            int64_t K, int group, cudaStream_t s);
 
+// Small-batch decode product, 2 <= M <= 8, bits 4 or 8, codes streamed into
+// shared memory; returns cudaErrorNotSupported (nothing launched) for shapes
+// outside its layout.
+cudaError_t launch_gemv_batch(const float *x, const uint32_t *codes, const uint16_t *scales,
+                              const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits,
+                              int group, cudaStream_t s);
+
 // Prefill product, bits == 4, group in {64, 128}, K % 64 == 0, M >= 1, N >= 1.
 cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
                         const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K,
@@ -42,5 +49,6 @@ cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uin
 cudaError_t read_clear_gemm_status(int *status, cudaStream_t s);
 cudaError_t read_clear_gemv_status(int *status, cudaStream_t s);
 cudaError_t read_clear_q1_status(int *status, cudaStream_t s);
+cudaError_t read_clear_batch_status(int *status, cudaStream_t s);
 
 }  // namespace qmm

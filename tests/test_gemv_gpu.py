@@ -151,3 +151,18 @@ def test_chained_products_see_the_previous_output(qmm):
         y2s = qmm.gemv(y1s, pb, tb["scales"], tb["biases"], N2, 4, 64)
         torch.cuda.synchronize()
         assert torch.equal(y2, y2s)
+
+
+# small-batch decode at MLP-projection shapes: several 32-row blocks per SM,
+# one or two token passes, ragged row blocks
+BATCH = [(2, 6144, 2048, 4, 64), (4, 6144, 2048, 4, 64), (8, 2048, 6144, 4, 64), (3, 8192, 4096, 8, 64),
+         (8, 8192, 1024, 8, 32), (5, 4100, 2048, 8, 128), (7, 1000, 4096, 4, 128)]
+
+
+@pytest.mark.parametrize("M,N,K,bits,group", BATCH)
+def test_small_batch_projection_shapes(qmm, oracle_mod, M, N, K, bits, group):
+    y, ref, t, p, d = run_case(qmm, oracle_mod, M, N, K, bits, group, seed=M + N + K)
+    assert np.all(np.abs(y - ref) <= fp32_bound(d, bits, group)), (M, N, K, bits, group)
+    assert rel_l2_rows(y, ref) <= TOL
+    y2 = qmm.gemv(t["x"], p, t["scales"], t["biases"], N, bits, group).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
