@@ -133,6 +133,41 @@ int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scal
              int group, qmm_stream_t stream);
 
 /*
+ * qmm_quantize -- INT4 affine quantization of float32 weights w[N, K] into the
+ *   stored format (packed codes, binary16 scales and biases per group), after
+ *   the quantization section of "I Built an LLM Inference Engine on a 15 year
+ *   old GPU and the Math was the Easy Part" ("Quantization: The Model Doesn't
+ *   Run on INT4": a block's min and max define the range, scale =
+ *   (max - min) / 15, q = round((w - min) / scale), dequantized = q * scale + min).
+ *   Per group, in float32: lo / hi = min / max of the group (NaN values
+ *   skipped, -0 ordered below +0), scale = binary16(RNE((hi - lo) / 15)),
+ *   bias = binary16(RNE(lo)), and q = clamp(round((w - bias) / scale), 0, 15)
+ *   with the stored coefficients, halves away from zero; q = 0 for a NaN
+ *   weight or when the stored scale is not positive and finite.  A NaN scale or
+ *   bias is stored as 0x7E00.  The result is the same on every run.
+ *   Layout: w [N, K] float32; packed, scales, biases as for the products.
+ *   Requires K % 32 == 0, group in {32, 64, 128}, K % group == 0.
+ */
+int qmm_quantize(const float *w, uint32_t *packed, uint16_t *scales, uint16_t *biases, int64_t N,
+                 int64_t K, int group, qmm_stream_t stream);
+
+/*
+ * qmm_gather_dequant -- out[t, :] = dequant(W[ids[t], :]) for t < T: rows of a
+ *   quantized table selected by token ids and decoded exactly (the embedding
+ *   lookup of a tied INT4 table, "Pushing the limits of legacy hardware",
+ *   section "Half a billion values, and one negative zero").  Each element is
+ *   computed as in qmm_dequant, so signed zeros and subnormal coefficients are
+ *   kept.  ids are int32 in device memory; an id outside [0, N) is not read
+ *   through and yields a row of quiet NaNs.
+ *   Layout: ids [T] int32, out [T, K] float32; packed, scales, biases as above.
+ *   Requires K % 32 == 0, K % group == 0; biases non-NULL iff bits == 4.
+ *   T == 0 is a no-op.
+ */
+int qmm_gather_dequant(const int32_t *ids, int64_t T, const uint32_t *packed, const uint16_t *scales,
+                       const uint16_t *biases, float *out, int64_t N, int64_t K, int bits, int group,
+                       qmm_stream_t stream);
+
+/*
  * qmm_check -- synchronize `stream`, then report QMM_ERR_CUDA if a kernel
  * failed, QMM_ERR_DEVICE_TIMEOUT if a bounded wait in a prefill kernel ran
  * out since the last qmm_check (and clear that record), else QMM_OK.

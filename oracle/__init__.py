@@ -19,4 +19,6 @@ from .oracle import (  # noqa: F401
     qmm_bf16x,
     qmm_sampled,
     quantize_affine4,
+    float_to_half,
+    quantize_affine4_f32,
 )

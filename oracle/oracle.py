@@ -59,6 +59,9 @@ def _load():
             lib.oracle_qmm_sampled.argtypes = [vp, i32, vp, vp, vp, vp, vp, i64, vp,
                                                i64, i64, i64, i32, i32]
             lib.oracle_quantize_affine4.argtypes = [vp, i64, vp, vp, vp]
+            lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+            lib.oracle_float_to_half.restype = ctypes.c_uint16
+            lib.oracle_quantize_affine4_f32.argtypes = [vp, i64, i64, i32, vp, vp, vp]
             for f in ("oracle_pack", "oracle_unpack", "oracle_dequant", "oracle_qmm_f32x",
                       "oracle_qmm_bf16x", "oracle_qmm_sampled", "oracle_quantize_affine4"):
                 getattr(lib, f).restype = i32
@@ -183,3 +186,21 @@ def quantize_affine4(w):
     _check(_load().oracle_quantize_affine4(_ptr(w), w.size, _ptr(q), ctypes.addressof(s),
                                            ctypes.addressof(mn)), "quantize_affine4")
     return q, s.value, mn.value
+
+
+def float_to_half(f: float) -> int:
+    """binary16 bit pattern of float32 f, round to nearest even (qmm_oracle.c)."""
+    return int(_load().oracle_float_to_half(ctypes.c_float(f)))
+
+
+def quantize_affine4_f32(w, group):
+    """(codes uint8 [N,K], scales uint16 [N,K/group], biases uint16) of float32 w [N,K]:
+    the stored-format INT4 affine quantizer of qmm_oracle.c."""
+    w = _arr(np.asarray(w, dtype=np.float32), np.float32)
+    N, K = w.shape
+    codes = np.empty((N, K), dtype=np.uint8)
+    sc = np.empty((N, K // group), dtype=np.uint16)
+    bi = np.empty((N, K // group), dtype=np.uint16)
+    _check(_load().oracle_quantize_affine4_f32(_ptr(w), N, K, group, _ptr(codes), _ptr(sc), _ptr(bi)),
+           "quantize_affine4_f32")
+    return codes, sc, bi

@@ -37,6 +37,7 @@
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
 /* ---------------------------------------------------------------- decoders */
 
@@ -70,6 +71,51 @@ double oracle_bf16_to_double(uint16_t b)
     else
         v = ldexp((double)(f + 128), e - 134);     /* (1 + f/2^7) * 2^(e-127) */
     return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------ encoders */
+
+/* float32 -> IEEE 754 binary16, round to nearest, ties to even; overflow to
+ * infinity, gradual underflow to subnormals, NaN to a quiet NaN with the
+ * sign kept (0x7E00 | sign).  Written from the two formats' bit layouts. */
+uint16_t oracle_float_to_half(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    int e = (int)((u >> 23) & 0xFF);
+    uint32_t m = u & 0x7FFFFFu;
+    if (e == 255) return (uint16_t)(sign | (m ? 0x7E00u : 0x7C00u));
+    if (e == 0 && m == 0) return sign;
+    /* value = sig * 2^(exp2) with sig an integer of up to 24 bits */
+    uint32_t sig = (e == 0) ? m : (m | 0x800000u);
+    int exp2 = (e == 0) ? -149 : e - 150;
+    /* target: binary16 value = hsig * 2^hexp, hexp >= -24 (subnormal step),
+     * normal numbers keep 11 significant bits */
+    int msb = 31;
+    while (!((sig >> msb) & 1u)) msb--;             /* position of the leading bit */
+    int top = exp2 + msb;                           /* value in [2^top, 2^(top+1)) */
+    int hexp = top - 10;                            /* ulp exponent for 11 bits */
+    if (hexp < -24) hexp = -24;                     /* subnormal range */
+    int shift = hexp - exp2;                        /* bits of sig to drop */
+    uint32_t q;
+    if (shift <= 0) {
+        q = sig << (-shift);                        /* exact */
+    } else if (shift > 31) {
+        q = 0;                                      /* far below half the smallest subnormal */
+    } else {
+        uint32_t rem = sig & ((1u << shift) - 1u);
+        uint32_t half = 1u << (shift - 1);
+        q = sig >> shift;
+        if (rem > half || (rem == half && (q & 1u))) q++;
+    }
+    /* q * 2^hexp; q may have carried to 2^11 (or reached 2^10 from a subnormal) */
+    if (q == 0) return sign;
+    int E = hexp + 25;                              /* biased exponent if q in [2^10, 2^11) */
+    if (q >= 2048u) { q >>= 1; E++; }               /* carry: q was exactly 2^11 */
+    if (q < 1024u) return (uint16_t)(sign | q);     /* subnormal (hexp == -24) */
+    if (E >= 31) return (uint16_t)(sign | 0x7C00u); /* overflow */
+    return (uint16_t)(sign | ((uint32_t)E << 10) | (q & 0x3FFu));
 }
 
 /* ------------------------------------------------------------ packing */
@@ -297,5 +343,60 @@ int oracle_quantize_affine4(const double *w, int64_t count, uint8_t *q, double *
     }
     *scale = s;
     *minv = lo;
+    return 0;
+}
+
+/* The quantizer as the library stores its output: INT4 affine codes with
+ * binary16 scale and bias per group of `group` consecutive k of a row.
+ * Per group, in float32 (every operation one IEEE float operation):
+ *   lo, hi  = min and max of the group's values (NaN values are skipped)
+ *   scale   = binary16(RNE((hi - lo) / 15)),  bias = binary16(RNE(lo))
+ *             (-0 orders below +0 in the min and max; a NaN scale or bias is
+ *             stored as 0x7E00)
+ *   q       = clamp(roundf((w - bias) / scale), 0, 15), halves away from zero,
+ *             taken with the stored (binary16) scale and bias, so that
+ *             q * scale + bias is the nearest level of the stored grid;
+ *             q = 0 when the stored scale is not positive and finite, or w is NaN.
+ * The float32 steps are the reading of the page's "round((w - min) / scale)"
+ * for a format that stores binary16 coefficients; the decision that picks the
+ * integer q is made in the same precision on the CPU and on the GPU. */
+int oracle_quantize_affine4_f32(const float *w, int64_t N, int64_t K, int group, uint8_t *codes,
+                                uint16_t *scales, uint16_t *biases)
+{
+    if (N < 0 || K < 0 || group <= 0 || K % group != 0) return -1;
+    int64_t G = K / group;
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t g = 0; g < G; g++) {
+            const float *v = w + n * K + g * group;
+            float lo = NAN, hi = NAN;
+            for (int i = 0; i < group; i++) {
+                float x = v[i];
+                if (isnan(x)) continue;
+                /* -0 counts as below +0, so the result does not depend on order */
+                if (isnan(lo) || x < lo || (x == lo && signbit(x) && !signbit(lo))) lo = x;
+                if (isnan(hi) || x > hi || (x == hi && !signbit(x) && signbit(hi))) hi = x;
+            }
+            volatile float range = hi - lo;
+            volatile float s32 = range / 15.0f;
+            uint16_t sh = isnan(s32) ? 0x7E00u : oracle_float_to_half(s32);
+            uint16_t bh = isnan(lo) ? 0x7E00u : oracle_float_to_half(lo);
+            float s = (float)oracle_half_to_double(sh), b = (float)oracle_half_to_double(bh);
+            scales[n * G + g] = sh;
+            biases[n * G + g] = bh;
+            for (int i = 0; i < group; i++) {
+                uint8_t c = 0;
+                if (s > 0.0f && isfinite(s) && !isnan(v[i])) {
+                    volatile float d = v[i] - b;
+                    volatile float t = d / s;
+                    float r = roundf(t);
+                    if (isnan(r)) r = 0.0f;
+                    if (r < 0.0f) r = 0.0f;
+                    if (r > 15.0f) r = 15.0f;
+                    c = (uint8_t)r;
+                }
+                codes[n * K + g * group + i] = c;
+            }
+        }
+    }
     return 0;
 }

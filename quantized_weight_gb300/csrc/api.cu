@@ -109,6 +109,31 @@ int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scal
   return cuda_status(qmm::launch_gemm(x_bf16, codes, scales, biases, y, M, N, K, group, stream));
 }
 
+int qmm_quantize(const float *w, uint32_t *packed, uint16_t *scales, uint16_t *biases, int64_t N,
+                 int64_t K, int group, qmm_stream_t stream) {
+  if (!group_ok(group)) return QMM_ERR_UNSUPPORTED;
+  if (N < 0 || K < 0 || K % 32 != 0 || K % group != 0 || N >= kMaxDim || K >= kMaxDim) return QMM_ERR_SHAPE;
+  if (N == 0 || K == 0) return QMM_OK;
+  if (!w || !packed || !scales || !biases) return QMM_ERR_ARG;
+  if (!aligned16(w) || !aligned16(packed) || !aligned16(scales) || !aligned16(biases)) return QMM_ERR_ALIGN;
+  return cuda_status(qmm::launch_quantize(w, packed, scales, biases, N, K, group, stream));
+}
+
+int qmm_gather_dequant(const int32_t *ids, int64_t T, const uint32_t *packed, const uint16_t *scales,
+                       const uint16_t *biases, float *out, int64_t N, int64_t K, int bits, int group,
+                       qmm_stream_t stream) {
+  if (!bits_ok(bits) || !group_ok(group)) return QMM_ERR_UNSUPPORTED;
+  if (T < 0 || N < 0 || K < 0 || K % 32 != 0 || K % group != 0 || T >= kMaxDim || N >= kMaxDim ||
+      K >= kMaxDim)
+    return QMM_ERR_SHAPE;
+  if (T == 0 || K == 0) return QMM_OK;
+  if (!ids || !packed || !out) return QMM_ERR_ARG;
+  int st = check_coeffs(scales, biases, bits);
+  if (st != QMM_OK) return st;
+  if (!aligned16(ids) || !aligned16(packed) || !aligned16(out)) return QMM_ERR_ALIGN;
+  return cuda_status(qmm::launch_gather_dequant(ids, T, packed, scales, biases, out, N, K, bits, group, stream));
+}
+
 int qmm_check(qmm_stream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return QMM_ERR_CUDA;
   int st[4] = {0, 0, 0, 0};

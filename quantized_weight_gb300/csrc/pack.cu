@@ -1,4 +1,4 @@
-// pack.cu -- pack / unpack / dequantize kernels.
+// pack.cu -- format kernels: pack / unpack / dequantize, row gather, quantize.
 //
 // Packing convention (the pages fix no bit order): element k of a row sits in
 // 32-bit word k / (32/bits) of that row, at bit offset bits * (k mod (32/bits)),
@@ -10,7 +10,10 @@
 // pack and unpack kernels need no row arithmetic.
 //
 // One thread handles one 32-bit word in a grid-stride loop; reads and writes
-// are contiguous across consecutive threads.
+// are contiguous across consecutive threads.  The same file holds the other
+// format kernels: row gather with dequantization and the INT4 quantizer.
+#include <cuda_fp16.h>
+
 #include "qmm_device.cuh"
 #include "qmm_launch.h"
 
@@ -97,6 +100,28 @@ __global__ void __launch_bounds__(kThreads) unpack_kernel(const uint32_t *__rest
 // bits), so a single rounded add gives the correctly rounded weight; the
 // explicit _rn intrinsics keep the compiler from contracting or reordering.
 template <int BITS>
+__device__ __forceinline__ void dequant_word(uint32_t w, float s, float b, float (&v)[32 / BITS]) {
+#pragma unroll
+  for (int j = 0; j < 32 / BITS; j++) {
+    uint32_t u = (w >> (BITS * j)) & ((1u << BITS) - 1u);
+    if (BITS == 4) {
+      v[j] = __fadd_rn(__fmul_rn(s, (float)u), b);
+    } else if (BITS == 8) {
+      v[j] = __fmul_rn(s, (float)(int)(int8_t)(uint8_t)u);
+    } else {
+      v[j] = u ? s : -s;                            // s * (2b - 1), exact
+    }
+  }
+}
+
+template <int PER>
+__device__ __forceinline__ void store_vec(float *out, const float (&v)[PER]) {
+  float4 *o = reinterpret_cast<float4 *>(out);
+#pragma unroll
+  for (int j = 0; j < PER / 4; j++) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
+template <int BITS>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(
     const uint32_t *__restrict__ packed, const uint16_t *__restrict__ scales,
     const uint16_t *__restrict__ biases, float *__restrict__ out, int64_t words,
@@ -107,24 +132,121 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(
     int64_t n = i / words_per_row;
     int64_t k0 = (i % words_per_row) * PER;
     int64_t gi = n * groups_per_row + k0 / group;   // a word never straddles a group
-    float s = h2f(scales[gi]);
-    float b = (BITS == 4) ? h2f(biases[gi]) : 0.0f;
-    uint32_t w = packed[i];
     float v[PER];
+    dequant_word<BITS>(packed[i], h2f(scales[gi]), (BITS == 4) ? h2f(biases[gi]) : 0.0f, v);
+    store_vec<PER>(out + i * PER, v);
+  }
+}
+
+// Row gather with dequantization: out[t, :] = dequant(W[ids[t], :]), the
+// embedding lookup of a tied INT4 table ("Pushing the limits of legacy
+// hardware", section "Half a billion values, and one negative zero": token ids
+// select rows that are decoded exactly).  Same element rule as dequant_kernel;
+// an id outside [0, N) yields a row of quiet NaNs (nothing is read for it).
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) gather_dequant_kernel(
+    const int32_t *__restrict__ ids, const uint32_t *__restrict__ packed, const uint16_t *__restrict__ scales,
+    const uint16_t *__restrict__ biases, float *__restrict__ out, int64_t items, int64_t N,
+    int64_t words_per_row, int64_t groups_per_row, int group) {
+  constexpr int PER = 32 / BITS;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / words_per_row, j = i % words_per_row;
+    const int64_t n = ids[t];
+    float v[PER];
+    if (n < 0 || n >= N) {
 #pragma unroll
-    for (int j = 0; j < PER; j++) {
-      uint32_t u = (w >> (BITS * j)) & ((1u << BITS) - 1u);
-      if (BITS == 4) {
-        v[j] = __fadd_rn(__fmul_rn(s, (float)u), b);
-      } else if (BITS == 8) {
-        v[j] = __fmul_rn(s, (float)(int)(int8_t)(uint8_t)u);
-      } else {
-        v[j] = u ? s : -s;                            // s * (2b - 1), exact
+      for (int e = 0; e < PER; e++) v[e] = __int_as_float(0x7FC00000);
+    } else {
+      const int64_t gi = n * groups_per_row + j * PER / group;
+      dequant_word<BITS>(packed[n * words_per_row + j], h2f(scales[gi]), (BITS == 4) ? h2f(biases[gi]) : 0.0f,
+                         v);
+    }
+    store_vec<PER>(out + i * PER, v);
+  }
+}
+
+// ---------------------------------------------------------------- quantizer
+
+// Total order on non-NaN floats for the group's range: -0 below +0, so the
+// stored bias does not depend on the order of the reduction.
+__device__ __forceinline__ float qmin(float a, float b) {
+  if (isnan(a)) return b;
+  if (isnan(b)) return a;
+  if (a < b) return a;
+  if (b < a) return b;
+  return signbit(a) ? a : b;
+}
+__device__ __forceinline__ float qmax(float a, float b) {
+  if (isnan(a)) return b;
+  if (isnan(b)) return a;
+  if (a > b) return a;
+  if (b > a) return b;
+  return signbit(a) ? b : a;
+}
+
+// binary16 bits of f, round to nearest even; any NaN becomes 0x7E00.
+__device__ __forceinline__ uint16_t half_bits_rn(float f) {
+  return isnan(f) ? (uint16_t)0x7E00u : __half_as_ushort(__float2half_rn(f));
+}
+
+// INT4 affine quantization of float32 weights to the stored format, after
+// the quantization section of "I Built an LLM Inference Engine on a 15 year
+// old GPU and the Math was the Easy Part": per group of consecutive k, the
+// range [min, max] is cut into 15 steps, scale = (max - min) / 15 and
+// bias = min are stored as binary16 (round to nearest even), and each weight
+// becomes q = clamp(round((w - bias) / scale), 0, 15) computed in float32
+// with the stored coefficients (halves away from zero; q = 0 for a NaN weight
+// or a scale that is not positive and finite).  One thread per 8 weights (one
+// code word); the GT = group/8 threads of a group are adjacent lanes of one
+// warp and reduce the range with shuffles.
+template <int GT>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const float *__restrict__ w,
+                                                             uint32_t *__restrict__ packed,
+                                                             uint16_t *__restrict__ scales,
+                                                             uint16_t *__restrict__ biases, int64_t words) {
+  const int lane = threadIdx.x & 31;
+  // the loop bound is uniform per warp so that every lane takes part in the shuffles
+  for (int64_t base = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) - lane; base < words;
+       base += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = base + lane;
+    const bool active = i < words;
+    float v[8];
+    if (active) {
+      const float4 a = reinterpret_cast<const float4 *>(w)[2 * i];
+      const float4 c = reinterpret_cast<const float4 *>(w)[2 * i + 1];
+      v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = c.x, v[5] = c.y, v[6] = c.z, v[7] = c.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; j++) v[j] = __int_as_float(0x7FC00000);
+    }
+    float lo = v[0], hi = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; j++) lo = qmin(lo, v[j]), hi = qmax(hi, v[j]);
+#pragma unroll
+    for (int o = 1; o < GT; o <<= 1) {
+      lo = qmin(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = qmax(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (!active) continue;
+    const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+    const uint16_t sh = half_bits_rn(s32), bh = half_bits_rn(lo);
+    const float s = h2f(sh), b = h2f(bh);
+    uint32_t word = 0;
+    if (s > 0.0f && isfinite(s)) {
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        if (isnan(v[j])) continue;
+        float r = roundf(__fdiv_rn(__fsub_rn(v[j], b), s));
+        r = fminf(fmaxf(r, 0.0f), 15.0f);
+        word |= (uint32_t)r << (4 * j);
       }
     }
-    float4 *o = reinterpret_cast<float4 *>(out + i * PER);
-#pragma unroll
-    for (int j = 0; j < PER / 4; j++) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    packed[i] = word;
+    if (lane % GT == 0) {
+      scales[i / GT] = sh;
+      biases[i / GT] = bh;
+    }
   }
 }
 
@@ -161,6 +283,32 @@ cudaError_t launch_dequant(const uint32_t *packed, const uint16_t *scales, const
   if (bits == 4) dequant_kernel<4><<<g, kThreads, 0, s>>>(packed, scales, biases, w, words, wpr, gpr, group);
   else if (bits == 8) dequant_kernel<8><<<g, kThreads, 0, s>>>(packed, scales, biases, w, words, wpr, gpr, group);
   else dequant_kernel<1><<<g, kThreads, 0, s>>>(packed, scales, biases, w, words, wpr, gpr, group);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_dequant(const int32_t *ids, int64_t T, const uint32_t *packed, const uint16_t *scales,
+                                  const uint16_t *biases, float *out, int64_t N, int64_t K, int bits, int group,
+                                  cudaStream_t s) {
+  const int64_t wpr = K * bits / 32, gpr = K / group, items = T * wpr;
+  if (items == 0) return cudaSuccess;
+  int g = grid_for(items);
+  if (bits == 4)
+    gather_dequant_kernel<4><<<g, kThreads, 0, s>>>(ids, packed, scales, biases, out, items, N, wpr, gpr, group);
+  else if (bits == 8)
+    gather_dequant_kernel<8><<<g, kThreads, 0, s>>>(ids, packed, scales, biases, out, items, N, wpr, gpr, group);
+  else
+    gather_dequant_kernel<1><<<g, kThreads, 0, s>>>(ids, packed, scales, biases, out, items, N, wpr, gpr, group);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const float *w, uint32_t *packed, uint16_t *scales, uint16_t *biases, int64_t N,
+                            int64_t K, int group, cudaStream_t s) {
+  const int64_t words = N * K / 8;
+  if (words == 0) return cudaSuccess;
+  int g = grid_for(words);
+  if (group == 32) quantize_kernel<4><<<g, kThreads, 0, s>>>(w, packed, scales, biases, words);
+  else if (group == 64) quantize_kernel<8><<<g, kThreads, 0, s>>>(w, packed, scales, biases, words);
+  else quantize_kernel<16><<<g, kThreads, 0, s>>>(w, packed, scales, biases, words);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,14 @@ cudaError_t launch_unpack(const uint32_t *packed, uint8_t *codes, int64_t N, int
 cudaError_t launch_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases,
                            float *w, int64_t N, int64_t K, int bits, int group, cudaStream_t s);
 
+// out[t, :] = dequant(W[ids[t], :]) for t < T; ids outside [0, N) give NaN rows.
+cudaError_t launch_gather_dequant(const int32_t *ids, int64_t T, const uint32_t *packed, const uint16_t *scales,
+                                  const uint16_t *biases, float *out, int64_t N, int64_t K, int bits, int group,
+                                  cudaStream_t s);
+// INT4 affine quantization of float32 w [N, K] (group in {32, 64, 128}).
+cudaError_t launch_quantize(const float *w, uint32_t *packed, uint16_t *scales, uint16_t *biases, int64_t N,
+                            int64_t K, int group, cudaStream_t s);
+
 // Decode product, 1 <= M <= 8, K > 0, N > 0.
 cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *scales,
                         const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits,

@@ -62,12 +62,14 @@ def lib():
             L.qmm_dequant.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, vp]
             L.qmm_gemv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
             L.qmm_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
+            L.qmm_quantize.argtypes = [vp, vp, vp, vp, i64, i64, i32, vp]
+            L.qmm_gather_dequant.argtypes = [vp, i64, vp, vp, vp, vp, i64, i64, i32, i32, vp]
             L.qmm_check.argtypes = [vp]
             L.qmm_status_string.argtypes = [i32]
             L.qmm_status_string.restype = ctypes.c_char_p
             L.qmm_abi_version.argtypes = []
-            for f in ("qmm_pack", "qmm_unpack", "qmm_dequant", "qmm_gemv", "qmm_gemm", "qmm_check",
-                      "qmm_abi_version"):
+            for f in ("qmm_pack", "qmm_unpack", "qmm_dequant", "qmm_gemv", "qmm_gemm", "qmm_quantize",
+                      "qmm_gather_dequant", "qmm_check", "qmm_abi_version"):
                 getattr(L, f).restype = i32
             _lib = L
     return _lib
@@ -170,6 +172,38 @@ def gemm(x, packed, scales, biases, N, bits, group, out=None, stream=None) -> to
     _need(out, "out", torch.float32, (M, N))
     _call("qmm_gemm", lib().qmm_gemm(_ptr(x), _ptr(packed), _ptr(scales), _ptr(biases), _ptr(out),
                                      M, N, K, bits, group, _stream(stream)))
+    return out
+
+
+def quantize(w, group=64, out=None, stream=None):
+    """INT4 affine quantization of float32 w [N, K]: (packed int32 [N, K/8],
+    scales float16 [N, K/group], biases float16 [N, K/group])."""
+    N, K = w.shape
+    _need(w, "w", torch.float32)
+    if out is None:
+        out = (torch.empty((N, K // 8), dtype=torch.int32, device=w.device),
+               torch.empty((N, K // group), dtype=torch.float16, device=w.device),
+               torch.empty((N, K // group), dtype=torch.float16, device=w.device))
+    packed, scales, biases = out
+    _need(packed, "packed", torch.int32, (N, K // 8))
+    _need(scales, "scales", torch.float16, (N, K // group))
+    _need(biases, "biases", torch.float16, (N, K // group))
+    _call("qmm_quantize", lib().qmm_quantize(_ptr(w), _ptr(packed), _ptr(scales), _ptr(biases), N, K, group,
+                                             _stream(stream)))
+    return packed, scales, biases
+
+
+def gather_dequant(ids, packed, scales, biases, N, K, bits, group, out=None, stream=None) -> torch.Tensor:
+    """out[t, :] = dequant(W[ids[t], :]); int32 ids [T]; an id outside [0, N) gives a NaN row."""
+    _need(ids, "ids", torch.int32)
+    T = ids.numel()
+    _need(packed, "packed", torch.int32, (N, K * bits // 32))
+    _coeffs(scales, biases, N, K, bits, group)
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.float32, device=packed.device)
+    _need(out, "out", torch.float32, (T, K))
+    _call("qmm_gather_dequant", lib().qmm_gather_dequant(_ptr(ids), T, _ptr(packed), _ptr(scales), _ptr(biases),
+                                                         _ptr(out), N, K, bits, group, _stream(stream)))
     return out
 
 

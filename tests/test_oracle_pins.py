@@ -303,6 +303,11 @@ MUTANTS = {
     "half subnormal": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     "last group skipped": ("for (int64_t g0 = 0; g0 < K; g0 += group)",
                            "for (int64_t g0 = 0; g0 + group < K; g0 += group)"),
+    "binary16 ties round up": ("if (rem > half || (rem == half && (q & 1u))) q++;", "if (rem >= half) q++;"),
+    "quantizer truncates": ("float r = roundf(t);", "float r = truncf(t);"),
+    "quantizer ignores the bias": ("volatile float d = v[i] - b;", "volatile float d = v[i];"),
+    "quantizer max skipped": ("if (isnan(hi) || x > hi || (x == hi && !signbit(x) && signbit(hi))) hi = x;",
+                              "if (isnan(hi)) hi = x;"),
 }
 
 
@@ -328,6 +333,23 @@ def _checks_fail_with(lib_file):
         sub = np.array([om.half_to_double(v) for v in range(1, 1024)])
         if not np.array_equal(sub, np.arange(1, 1024, dtype=np.uint16).view(np.float16).astype(np.float64)):
             fails += 1
+        # binary16 encoder: ties to even, overflow, the subnormal edge
+        for v, want in [(1.0 + 2.0 ** -11, 0x3C00), (1.0 + 3 * 2.0 ** -11, 0x3C02), (65520.0, 0x7C00),
+                        (2.0 ** -25, 0x0000), (3 * 2.0 ** -26, 0x0001)]:
+            if om.float_to_half(v) != want:
+                fails += 1
+        # stored-format quantizer: an exact grid, and half a step of error at most
+        j = np.arange(64) % 16
+        j[1] = 15
+        w = (np.float32(-1.0) + j.astype(np.float32) * np.float32(0.0625))[None, :]
+        c, sh, bh = om.quantize_affine4_f32(np.ascontiguousarray(w), 64)
+        if not np.array_equal(c[0], j):
+            fails += 1
+        wr = np.random.default_rng(3).standard_normal((8, 128)).astype(np.float32)
+        c, sh, bh = om.quantize_affine4_f32(wr, 64)
+        s = sh.view(np.float16).astype(np.float64).repeat(64, axis=1)
+        if (np.abs(_dq(c, sh, bh, 64) - wr) > s * 0.5 + 2.0 ** -10).any():
+            fails += 1
         return fails > 0
     finally:
         om._lib, om._LIB = saved
@@ -344,3 +366,82 @@ def test_pins_catch_planted_mistakes(tmp_path, name):
     from oracle.oracle import CFLAGS
     subprocess.run(["gcc", *CFLAGS, str(mut), "-o", str(so), "-lm"], check=True)
     assert _checks_fail_with(str(so)), f"planted mistake {name!r} passed every pin"
+
+
+# ---------------------------------------------------------------- binary16 encoder and stored-format quantizer
+
+def test_float_to_half_rounds_like_numpy_at_every_boundary(oracle_mod):
+    """The oracle's own float32 -> binary16 encoder against numpy's cast (IEEE
+    round to nearest even) at every tie between adjacent binary16 values and
+    one float32 step on either side of it, plus the overflow edge."""
+    h = np.arange(0, 0x7C00, dtype=np.uint16)                # finite non-negative halves
+    lo = h[:-1].view(np.float16).astype(np.float64)
+    hi = h[1:].view(np.float16).astype(np.float64)
+    mid = ((lo + hi) / 2).astype(np.float32)                  # exact: 11 bits fit in 24
+    cand = np.concatenate([mid, np.nextafter(mid, np.float32(np.inf)), np.nextafter(mid, np.float32(0)),
+                           h.view(np.float16).astype(np.float32),
+                           np.array([65504.0, 65519.996, 65520.0, 1e9, 2.0 ** -25, 2.0 ** -26, 1e-30],
+                                    dtype=np.float32)])
+    cand = np.concatenate([cand, -cand])
+    rng = np.random.default_rng(7)
+    cand = cand[rng.permutation(cand.size)[:60000]]
+    with np.errstate(over="ignore"):
+        ref = cand.astype(np.float16).view(np.uint16)
+    got = np.array([oracle_mod.float_to_half(float(v)) for v in cand], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+    assert oracle_mod.float_to_half(float("nan")) == 0x7E00
+    assert oracle_mod.float_to_half(float("inf")) == 0x7C00
+    assert oracle_mod.float_to_half(-0.0) == 0x8000
+
+
+def _dq(codes, sh, bh, group):
+    s = sh.view(np.float16).astype(np.float64).repeat(group, axis=1)
+    b = bh.view(np.float16).astype(np.float64).repeat(group, axis=1)
+    return codes.astype(np.float64) * s + b
+
+
+def test_stored_quantizer_reproduces_the_worked_example(oracle_mod):
+    g = _golden("affine_worked_example.txt")
+    w = np.full((1, 64), g["weight"], dtype=np.float32)
+    w[0, 0], w[0, 1] = g["block_min"], g["block_max"]
+    codes, sh, bh = oracle_mod.quantize_affine4_f32(w, 64)
+    assert round(float(sh.view(np.float16)[0, 0]), 4) == g["scale"]
+    assert bh.view(np.float16)[0, 0] == np.float16(g["block_min"])
+    assert codes[0, 0] == g["code_of_min"] and codes[0, 1] == g["code_of_max"] and codes[0, 2] == g["code"]
+    assert round(_dq(codes, sh, bh, 64)[0, 2], 2) == g["dequantized"]
+
+
+def test_stored_quantizer_on_an_exact_grid(oracle_mod):
+    """Values lo + j*s with s and lo exact in binary16 and every step exact in
+    float32 quantize to q = j exactly, for every group size."""
+    for group in (32, 64, 128):
+        j = np.arange(group) % 16
+        j[0], j[1] = 0, 15                                    # the range is exactly 15 steps
+        w = (np.float32(-1.0) + j.astype(np.float32) * np.float32(0.0625))[None, :].repeat(3, axis=0)
+        w[1] *= np.float32(4.0)                              # s = 0.25, lo = -4
+        w[2] += np.float32(3.0)                              # lo = 2
+        codes, sh, bh = oracle_mod.quantize_affine4_f32(np.ascontiguousarray(w), group)
+        assert np.array_equal(codes, np.broadcast_to(j, w.shape))
+        assert list(sh.view(np.float16)[:, 0]) == [0.0625, 0.25, 0.0625]
+        assert list(bh.view(np.float16)[:, 0]) == [-1.0, -4.0, 2.0]
+
+
+def test_stored_quantizer_constant_nan_and_bounds(oracle_mod):
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((64, 256)).astype(np.float32)
+    w[0, :64] = 0.75                                          # constant group: scale 0, codes 0
+    w[1, 5] = np.nan                                          # NaN is skipped, coded 0
+    codes, sh, bh = oracle_mod.quantize_affine4_f32(w, 64)
+    assert sh[0, 0] == 0 and (codes[0, :64] == 0).all() and bh.view(np.float16)[0, 0] == 0.75
+    assert codes[1, 5] == 0
+    assert codes.max() <= 15
+    # every weight within half a step of its level (plus the binary16 rounding of the bias)
+    s = sh.view(np.float16).astype(np.float64).repeat(64, axis=1)
+    err = np.abs(_dq(codes, sh, bh, 64) - w)
+    ok = ~np.isnan(w)
+    ok[0, :64] = False
+    assert (err[ok] <= s[ok] * 0.5 + 2.0 ** -10).all()
+    # monotone: a sorted group gets non-decreasing codes
+    ws = np.sort(w[2:3], axis=1)
+    c2, _, _ = oracle_mod.quantize_affine4_f32(ws, 64)
+    assert (np.diff(c2.reshape(-1, 64), axis=1) >= 0).all()
