@@ -50,6 +50,7 @@
 #ifndef QMM_H
 #define QMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -131,6 +132,29 @@ int qmm_gemv(const float *x, const uint32_t *codes, const uint16_t *scales,
 int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
              const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int bits,
              int group, qmm_stream_t stream);
+
+/*
+ * qmm_gemv_argmax -- greedy decode head: idx[m] = argmax_n y[m, n] of the
+ *   decode product y = x * dequant(W)^T (qmm_gemv's arithmetic and shape
+ *   rules, 1 <= M <= 8), and val[m] = y[m, idx[m]] if val is not NULL.  The
+ *   fused greedy head of "Pushing the limits of legacy hardware", section
+ *   "Build the execution path, then share the weights": each tile keeps its
+ *   maximum with the original index and the tiles are reduced to one winner,
+ *   so the logits need not be written (at M == 1 the product's epilogue does
+ *   this and no logit is stored; otherwise the logits go to the workspace and
+ *   a reduction kernel follows).  Order: a NaN logit ranks first, then the
+ *   larger value, equal values to the lower index; the result is the same on
+ *   every run.
+ *   workspace: device memory of at least qmm_gemv_argmax_workspace_size(M, N)
+ *   bytes, 16-byte aligned, owned by the caller, whose first 16 bytes are zero
+ *   before the first call (for instance from cudaMemset); every call leaves
+ *   them zero again.  Two calls in flight at the same time must not share a
+ *   workspace.  idx: int32 [M]; val: float32 [M] or NULL.
+ */
+size_t qmm_gemv_argmax_workspace_size(int64_t M, int64_t N);
+int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
+                    const uint16_t *biases, int32_t *idx, float *val, int64_t M, int64_t N, int64_t K,
+                    int bits, int group, void *workspace, size_t workspace_bytes, qmm_stream_t stream);
 
 /*
  * qmm_quantize -- INT4 affine quantization of float32 weights w[N, K] into the

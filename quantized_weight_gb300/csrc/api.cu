@@ -19,6 +19,10 @@ constexpr int64_t kMaxDim = (int64_t)1 << 31;   // N, K, M each fit in int for t
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
+// Argmax workspace: a 16-byte counter slot, then per-CTA winners (values,
+// indices), then room for logits when the unfused path runs.
+constexpr size_t kArgmaxHead = 16 + 8 * (size_t)qmm::kArgmaxMaxCtas;
+
 // Shared checks for the entries that take codes + coefficients.
 int check_coeffs(const uint16_t *scales, const uint16_t *biases, int bits) {
   if (!scales) return QMM_ERR_ARG;
@@ -107,6 +111,36 @@ int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scal
   if (st != QMM_OK) return st;
   if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(y)) return QMM_ERR_ALIGN;
   return cuda_status(qmm::launch_gemm(x_bf16, codes, scales, biases, y, M, N, K, group, stream));
+}
+
+size_t qmm_gemv_argmax_workspace_size(int64_t M, int64_t N) {
+  if (M < 0 || N < 0) return 0;
+  return (size_t)kArgmaxHead + (size_t)M * (size_t)N * sizeof(float);
+}
+
+int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                    int32_t *idx, float *val, int64_t M, int64_t N, int64_t K, int bits, int group,
+                    void *workspace, size_t workspace_bytes, qmm_stream_t stream) {
+  if (!bits_ok(bits) || !group_ok(group)) return QMM_ERR_UNSUPPORTED;
+  if (M < 1 || M > 8 || N < 1 || K < 32 || K % 32 != 0 || K % group != 0 || N >= kMaxDim || K >= kMaxDim)
+    return QMM_ERR_SHAPE;
+  if (bits == 1 && K % 128 != 0) return QMM_ERR_SHAPE;
+  if (!x || !codes || !idx || !workspace) return QMM_ERR_ARG;
+  int st = check_coeffs(scales, biases, bits);
+  if (st != QMM_OK) return st;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(workspace) || !aligned16(idx)) return QMM_ERR_ALIGN;
+  if (workspace_bytes < qmm_gemv_argmax_workspace_size(M, N)) return QMM_ERR_SHAPE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (M == 1) {
+    qmm::ArgmaxWork w{reinterpret_cast<unsigned *>(ws), reinterpret_cast<float *>(ws + 16),
+                      reinterpret_cast<int32_t *>(ws + 16 + 4 * qmm::kArgmaxMaxCtas), idx, val};
+    cudaError_t e = qmm::launch_gemv_stream_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+  }
+  float *logits = reinterpret_cast<float *>(ws + kArgmaxHead);
+  cudaError_t e = qmm::launch_gemv(x, codes, scales, biases, logits, (int)M, N, K, bits, group, stream);
+  if (e != cudaSuccess) return QMM_ERR_CUDA;
+  return cuda_status(qmm::launch_argmax_rows(logits, (int)M, N, idx, val, stream));
 }
 
 int qmm_quantize(const float *w, uint32_t *packed, uint16_t *scales, uint16_t *biases, int64_t N,

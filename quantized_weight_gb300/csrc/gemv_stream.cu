@@ -33,6 +33,7 @@
 // Every mbarrier wait is bounded (bounded_wait.cuh); a wait that runs out
 // aborts the CTA, drains its outstanding copies and records
 // QMM_ERR_DEVICE_TIMEOUT for qmm_check().
+#include "argmax.cuh"
 #include "bounded_wait.cuh"
 #include "qmm_device.cuh"
 #include "qmm_launch.h"
@@ -75,7 +76,8 @@ struct StreamParams {
   int stages;          // ring depth
   int rows_per_cta;
   // shared-memory layout (bytes from the 128-byte-aligned base)
-  int off_coef, off_x, off_red, off_bar;
+  int off_coef, off_x, off_red, off_bar, off_am;
+  ArgmaxWork am;       // used by the argmax epilogue only
 };
 
 // INT4, two rows at once; see the file comment.  x pairs per word:
@@ -170,7 +172,9 @@ __device__ __forceinline__ int pair_of(int j, int &slot) {
   }
 }
 
-template <int BITS>
+// ARGMAX: instead of storing y, the epilogue reduces this CTA's rows to their
+// greedy argmax and the last CTA combines the CTAs' winners (argmax.cuh).
+template <int BITS, bool ARGMAX>
 __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams p) {
   using L = Lane<BITS>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -338,9 +342,24 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(done_bar);
-  if (!ok) return;
   // one thread per row adds the segment totals in segment order
-  if (!__all_sync(0xffffffffu, wait_bounded(done_bar, 0, ctl))) return;
+  const bool fin = ok && __all_sync(0xffffffffu, wait_bounded(done_bar, 0, ctl));
+  if constexpr (ARGMAX) {
+    // every consumer warp takes part, also after an abort (with no candidate),
+    // so the CTA barrier inside completes and the CTA is counted
+    float bv = __int_as_float(0xFF800000);
+    int bi = 0x7FFFFFFF;
+    if (fin) {
+      for (int r = ct; r < rows; r += nthreads) {
+        float acc = 0.0f;
+        for (int q = 0; q < p.segs; q++) acc += red[r * p.segs + q];
+        if (am_better(acc, n_begin + r, bv, bi)) bv = acc, bi = n_begin + r;
+      }
+    }
+    am_cta_finish(bv, bi, 1, consumers, reinterpret_cast<uint32_t *>(smem + p.off_am), 1, nthreads, p.am);
+    return;
+  }
+  if (!fin) return;
   for (int r = ct; r < rows; r += nthreads) {
     float acc = 0.0f;
     for (int q = 0; q < p.segs; q++) acc += red[r * p.segs + q];
@@ -391,7 +410,8 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   p.off_x = (p.off_coef + coef + 15) & ~15;
   p.off_red = p.off_x + xbytes;
   p.off_bar = (p.off_red + redb + 7) & ~7;
-  smem = (size_t)p.off_bar + 8 * (2 * S + 2) + 16;
+  p.off_am = (p.off_bar + 8 * (2 * S + 2) + 16 + 15) & ~15;
+  smem = (size_t)p.off_am + 8 * 16;
   int wps = kMaxConsumerWarps / p.segs;
   const int ngroups = (p.rows_per_cta + RG - 1) / RG;
   if (wps > ngroups) wps = ngroups;
@@ -401,9 +421,9 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   return true;
 }
 
-template <int BITS>
+template <int BITS, bool ARGMAX>
 cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t smem, cudaStream_t s) {
-  auto kern = gemv_stream_kernel<BITS>;
+  auto kern = gemv_stream_kernel<BITS, ARGMAX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // Every instantiation asks for the same (largest) shared-memory carveout, so
@@ -445,9 +465,30 @@ cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint
             : bits == 8 ? plan<8>(N, K, group, p, grid, threads, smem)
                         : plan<1>(N, K, group, p, grid, threads, smem);
   if (!ok) return cudaErrorNotSupported;
-  if (bits == 4) return launch_stream<4>(p, grid, threads, smem, s);
-  if (bits == 8) return launch_stream<8>(p, grid, threads, smem, s);
-  return launch_stream<1>(p, grid, threads, smem, s);
+  if (bits == 4) return launch_stream<4, false>(p, grid, threads, smem, s);
+  if (bits == 8) return launch_stream<8, false>(p, grid, threads, smem, s);
+  return launch_stream<1, false>(p, grid, threads, smem, s);
+}
+
+cudaError_t launch_gemv_stream_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
+                                      const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
+                                      const ArgmaxWork &w, cudaStream_t s) {
+  StreamParams p{};
+  p.x = x;
+  p.codes = reinterpret_cast<const uint8_t *>(codes);
+  p.scales = scales;
+  p.biases = biases;
+  p.y = nullptr;
+  p.am = w;
+  int grid = 0, threads = 0;
+  size_t smem = 0;
+  bool ok = bits == 4 ? plan<4>(N, K, group, p, grid, threads, smem)
+            : bits == 8 ? plan<8>(N, K, group, p, grid, threads, smem)
+                        : plan<1>(N, K, group, p, grid, threads, smem);
+  if (!ok || grid > kArgmaxMaxCtas) return cudaErrorNotSupported;
+  if (bits == 4) return launch_stream<4, true>(p, grid, threads, smem, s);
+  if (bits == 8) return launch_stream<8, true>(p, grid, threads, smem, s);
+  return launch_stream<1, true>(p, grid, threads, smem, s);
 }
 
 cudaError_t read_clear_gemv_status(int *status, cudaStream_t s) {

@@ -9,6 +9,16 @@
 
 namespace qmm {
 
+// Work area of a fused greedy-argmax decode product (device memory).
+struct ArgmaxWork {
+  unsigned *counter;      // CTAs finished in this call: 0 before a call, reset to 0 by its last CTA
+  float *part_val;        // [grid] per-CTA winners
+  int32_t *part_idx;
+  int32_t *out_idx;       // the result (one token)
+  float *out_val;         // may be null
+};
+constexpr int kArgmaxMaxCtas = 1024;
+
 cudaError_t launch_pack(const uint8_t *codes, uint32_t *packed, int64_t N, int64_t K, int bits,
                         cudaStream_t s);
 cudaError_t launch_unpack(const uint32_t *packed, uint8_t *codes, int64_t N, int64_t K, int bits,
@@ -34,6 +44,14 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
 cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint16_t *scales,
                                const uint16_t *biases, float *y, int64_t N, int64_t K, int bits, int group,
                                cudaStream_t s);
+
+// M == 1 decode product whose epilogue keeps only the argmax of y (no y is
+// written); cudaErrorNotSupported (nothing launched) outside the streaming layout.
+cudaError_t launch_gemv_stream_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
+                                      const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
+                                      const ArgmaxWork &w, cudaStream_t s);
+// Per row m < M of logits [M, N]: idx[m] = argmax (NaN first, ties to the lower index), val[m] its value.
+cudaError_t launch_argmax_rows(const float *logits, int M, int64_t N, int32_t *idx, float *val, cudaStream_t s);
 
 // Binary (Q1) decode product for M == 1 through per-chunk lookup tables;
 // returns cudaErrorNotSupported (nothing launched) for shapes outside its layout.

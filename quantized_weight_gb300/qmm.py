@@ -64,12 +64,15 @@ def lib():
             L.qmm_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
             L.qmm_quantize.argtypes = [vp, vp, vp, vp, i64, i64, i32, vp]
             L.qmm_gather_dequant.argtypes = [vp, i64, vp, vp, vp, vp, i64, i64, i32, i32, vp]
+            L.qmm_gemv_argmax_workspace_size.argtypes = [i64, i64]
+            L.qmm_gemv_argmax_workspace_size.restype = ctypes.c_size_t
+            L.qmm_gemv_argmax.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, ctypes.c_size_t, vp]
             L.qmm_check.argtypes = [vp]
             L.qmm_status_string.argtypes = [i32]
             L.qmm_status_string.restype = ctypes.c_char_p
             L.qmm_abi_version.argtypes = []
             for f in ("qmm_pack", "qmm_unpack", "qmm_dequant", "qmm_gemv", "qmm_gemm", "qmm_quantize",
-                      "qmm_gather_dequant", "qmm_check", "qmm_abi_version"):
+                      "qmm_gather_dequant", "qmm_gemv_argmax", "qmm_check", "qmm_abi_version"):
                 getattr(L, f).restype = i32
             _lib = L
     return _lib
@@ -173,6 +176,31 @@ def gemm(x, packed, scales, biases, N, bits, group, out=None, stream=None) -> to
     _call("qmm_gemm", lib().qmm_gemm(_ptr(x), _ptr(packed), _ptr(scales), _ptr(biases), _ptr(out),
                                      M, N, K, bits, group, _stream(stream)))
     return out
+
+
+def argmax_workspace(M: int, N: int, device="cuda") -> torch.Tensor:
+    """A zeroed work area for gemv_argmax (reusable: every call leaves it ready)."""
+    n = int(lib().qmm_gemv_argmax_workspace_size(M, N))
+    return torch.zeros(((n + 15) // 16 * 16,), dtype=torch.uint8, device=device)
+
+
+def gemv_argmax(x, packed, scales, biases, N, bits, group, workspace, idx=None, val=None, stream=None):
+    """Greedy head: (idx int32 [M], val float32 [M]) of argmax_n (x . dequant(W)^T)[m, n]."""
+    M, K = x.shape
+    _need(x, "x", torch.float32)
+    _need(packed, "packed", torch.int32, (N, K * bits // 32))
+    _coeffs(scales, biases, N, K, bits, group)
+    _need(workspace, "workspace", torch.uint8)
+    if idx is None:
+        idx = torch.empty((M,), dtype=torch.int32, device=x.device)
+    if val is None:
+        val = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(idx, "idx", torch.int32, (M,))
+    _need(val, "val", torch.float32, (M,))
+    _call("qmm_gemv_argmax", lib().qmm_gemv_argmax(_ptr(x), _ptr(packed), _ptr(scales), _ptr(biases), _ptr(idx),
+                                                   _ptr(val), M, N, K, bits, group, _ptr(workspace),
+                                                   workspace.numel(), _stream(stream)))
+    return idx, val
 
 
 def quantize(w, group=64, out=None, stream=None):

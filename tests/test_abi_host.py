@@ -22,7 +22,8 @@ def L():
 def test_exports_every_declared_symbol(L):
     names = qmm.declared_symbols()
     assert {"qmm_pack", "qmm_unpack", "qmm_dequant", "qmm_gemv", "qmm_gemm", "qmm_check",
-            "qmm_status_string", "qmm_abi_version"} <= set(names)
+            "qmm_status_string", "qmm_abi_version", "qmm_quantize", "qmm_gather_dequant", "qmm_gemv_argmax",
+            "qmm_gemv_argmax_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(L, n), f"{n} declared in qmm.h but not exported"
     assert L.qmm_abi_version() == 1
@@ -96,3 +97,38 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qmm, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         qmm.lib()
+
+
+def argmax(L, x=FAKE, c=FAKE, s=FAKE, b=FAKE, i=FAKE, v=FAKE, M=1, N=64, K=128, bits=4, g=64, ws=FAKE,
+           nbytes=1 << 20):
+    return L.qmm_gemv_argmax(x, c, s, b, i, v, M, N, K, bits, g, ws, nbytes, None)
+
+
+def test_argmax_validation(L):
+    need = L.qmm_gemv_argmax_workspace_size(2, 1000)
+    assert need >= 2 * 1000 * 4 + 16
+    assert L.qmm_gemv_argmax_workspace_size(-1, 5) == 0
+    assert argmax(L, bits=3) == UNSUP
+    assert argmax(L, M=0) == SHAPE                 # a greedy head needs at least one token
+    assert argmax(L, M=9) == SHAPE
+    assert argmax(L, N=0) == SHAPE
+    assert argmax(L, K=0) == SHAPE
+    assert argmax(L, i=None) == ARG
+    assert argmax(L, ws=None) == ARG
+    assert argmax(L, b=None) == ARG
+    assert argmax(L, ws=MIS) == ALIGN
+    assert argmax(L, i=MIS) == ALIGN
+    assert argmax(L, M=2, N=1000, nbytes=need - 1) == SHAPE   # workspace too small
+
+
+def test_quantize_gather_validation(L):
+    assert L.qmm_quantize(FAKE, FAKE, FAKE, FAKE, 4, 64, 16, None) == UNSUP
+    assert L.qmm_quantize(FAKE, FAKE, FAKE, FAKE, 4, 96, 64, None) == SHAPE
+    assert L.qmm_quantize(FAKE, FAKE, FAKE, None, 4, 64, 64, None) == ARG
+    assert L.qmm_quantize(MIS, FAKE, FAKE, FAKE, 4, 64, 64, None) == ALIGN
+    assert L.qmm_quantize(FAKE, FAKE, FAKE, FAKE, 0, 64, 64, None) == OK
+    assert L.qmm_gather_dequant(FAKE, -1, FAKE, FAKE, FAKE, FAKE, 4, 64, 4, 64, None) == SHAPE
+    assert L.qmm_gather_dequant(FAKE, 3, FAKE, FAKE, None, FAKE, 4, 64, 4, 64, None) == ARG
+    assert L.qmm_gather_dequant(FAKE, 3, FAKE, FAKE, FAKE, FAKE, 4, 64, 8, 64, None) == ARG
+    assert L.qmm_gather_dequant(MIS, 3, FAKE, FAKE, FAKE, FAKE, 4, 64, 4, 64, None) == ALIGN
+    assert L.qmm_gather_dequant(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 4, 64, 4, 64, None) == OK
