@@ -157,6 +157,28 @@ int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scale
                     int bits, int group, void *workspace, size_t workspace_bytes, qmm_stream_t stream);
 
 /*
+ * qmm_gemv_argmax_noalloc -- qmm_gemv_argmax for M == 1 without a work area:
+ *   the same fused kernel and the same result (idx[0], and val[0] if val is
+ *   not NULL), with the CTA counter and per-CTA winners kept in a fixed
+ *   static device array of this library (8208 bytes: a 16-byte counter slot
+ *   and the winners of at most 1024 CTAs) instead of caller memory.  The pages
+ *   have no counterpart of this entry point: it exists for callers that cannot
+ *   allocate device memory at the call (a decode loop that must stay out of
+ *   the allocator between tokens, or a C host without an allocator).
+ *   Rules: the array's counter is zero when the library loads and every call
+ *   leaves it zero; the first call on each device looks the array's address
+ *   up (cudaGetSymbolAddress) and caches it, so make that first call before
+ *   any stream capture begins; all calls on a device share the array, so no
+ *   two calls may be in flight at once (calls in order on one stream are
+ *   fine).  Shapes that the fused M == 1 kernel does not take, or that would
+ *   need more than 1024 CTAs, return QMM_ERR_UNSUPPORTED.  Other argument
+ *   rules as qmm_gemv_argmax.
+ */
+int qmm_gemv_argmax_noalloc(const float *x, const uint32_t *codes, const uint16_t *scales,
+                            const uint16_t *biases, int32_t *idx, float *val, int64_t N, int64_t K,
+                            int bits, int group, qmm_stream_t stream);
+
+/*
  * qmm_quantize -- INT4 affine quantization of float32 weights w[N, K] into the
  *   stored format (packed codes, binary16 scales and biases per group), after
  *   the quantization section of "I Built an LLM Inference Engine on a 15 year

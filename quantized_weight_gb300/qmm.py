@@ -67,12 +67,14 @@ def lib():
             L.qmm_gemv_argmax_workspace_size.argtypes = [i64, i64]
             L.qmm_gemv_argmax_workspace_size.restype = ctypes.c_size_t
             L.qmm_gemv_argmax.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, ctypes.c_size_t, vp]
+            L.qmm_gemv_argmax_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, vp]
             L.qmm_check.argtypes = [vp]
             L.qmm_status_string.argtypes = [i32]
             L.qmm_status_string.restype = ctypes.c_char_p
             L.qmm_abi_version.argtypes = []
             for f in ("qmm_pack", "qmm_unpack", "qmm_dequant", "qmm_gemv", "qmm_gemm", "qmm_quantize",
-                      "qmm_gather_dequant", "qmm_gemv_argmax", "qmm_check", "qmm_abi_version"):
+                      "qmm_gather_dequant", "qmm_gemv_argmax", "qmm_gemv_argmax_noalloc", "qmm_check",
+                      "qmm_abi_version"):
                 getattr(L, f).restype = i32
             _lib = L
     return _lib
@@ -200,6 +202,25 @@ def gemv_argmax(x, packed, scales, biases, N, bits, group, workspace, idx=None, 
     _call("qmm_gemv_argmax", lib().qmm_gemv_argmax(_ptr(x), _ptr(packed), _ptr(scales), _ptr(biases), _ptr(idx),
                                                    _ptr(val), M, N, K, bits, group, _ptr(workspace),
                                                    workspace.numel(), _stream(stream)))
+    return idx, val
+
+
+def gemv_argmax_noalloc(x, packed, scales, biases, N, bits, group, idx=None, val=None, stream=None):
+    """gemv_argmax for one token with the library's static work area (no workspace argument)."""
+    M, K = x.shape
+    if M != 1:
+        raise ValueError("gemv_argmax_noalloc takes one token (M == 1)")
+    _need(x, "x", torch.float32)
+    _need(packed, "packed", torch.int32, (N, K * bits // 32))
+    _coeffs(scales, biases, N, K, bits, group)
+    if idx is None:
+        idx = torch.empty((1,), dtype=torch.int32, device=x.device)
+    if val is None:
+        val = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _need(idx, "idx", torch.int32, (1,))
+    _need(val, "val", torch.float32, (1,))
+    _call("qmm_gemv_argmax_noalloc", lib().qmm_gemv_argmax_noalloc(
+        _ptr(x), _ptr(packed), _ptr(scales), _ptr(biases), _ptr(idx), _ptr(val), N, K, bits, group, _stream(stream)))
     return idx, val
 
 
