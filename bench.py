@@ -245,6 +245,62 @@ def measure_config(name, torch, qmm, stream, pk, reps=20):
     return out
 
 
+EXTRA_WORKLOADS = {
+    # greedy argmax over the tied output head (no logits written): weight-GB/s
+    "head_argmax_int4_m1_k2048_n151936": ("argmax", 1, 151936, 2048),
+    # stored-format INT4 quantization of a 2B-class up-projection: bytes read + written per second
+    "quantize_int4_g64_k2048_n6144": ("quantize", 0, 6144, 2048),
+    # embedding lookup of 256 token ids in the tied INT4 table: bytes read + written per second
+    "gather_dequant_int4_t256_k2048_n151936": ("gather", 256, 151936, 2048),
+}
+
+
+def measure_extra(name, torch, qmm, stream, pk, reps=20):
+    """Per-launch time of the quantizer, gather and greedy-head entry points
+    (inputs in HBM, copies larger than L2 where the inputs are reused)."""
+    kind, M, N, K = EXTRA_WORKLOADS[name]
+    L2 = l2_bytes(torch)
+    if kind == "argmax":
+        d = inputs.make(1, N, K, 4, 64, 0)
+        t = {"x": torch.from_numpy(d["x"]).cuda(),
+             "packed": qmm.pack(torch.from_numpy(d["codes"]).cuda(), 4),
+             "scales": torch.from_numpy(d["scales"].view(np.float16)).cuda(),
+             "biases": torch.from_numpy(d["biases"].view(np.float16)).cuda()}
+        nbytes = gemv_bytes(1, N, K, 4, 64) - 4 * N          # no logits are written
+        copies = max(2, -(-4 * L2 // nbytes))
+        ts = replicate(t, copies, torch)
+        ws = [qmm.argmax_workspace(1, N) for _ in range(copies)]
+        calls = [(lambda i=i: qmm.gemv_argmax(ts[i]["x"], ts[i]["packed"], ts[i]["scales"], ts[i]["biases"], N, 4,
+                                              64, ws[i])) for i in range(copies)]
+    elif kind == "quantize":
+        w = torch.randn((N, K), device="cuda", generator=torch.Generator("cuda").manual_seed(0)) * 0.05
+        nbytes = N * K * 4 + N * K // 2 + N * (K // 64) * 4
+        copies = max(2, -(-4 * L2 // nbytes))
+        ws = [w.clone() for _ in range(copies)]
+        outs = [(torch.empty((N, K // 8), dtype=torch.int32, device="cuda"),
+                 torch.empty((N, K // 64), dtype=torch.float16, device="cuda"),
+                 torch.empty((N, K // 64), dtype=torch.float16, device="cuda")) for _ in range(copies)]
+        calls = [(lambda i=i: qmm.quantize(ws[i], 64, out=outs[i])) for i in range(copies)]
+    else:
+        d = inputs.make(1, N, K, 4, 64, 0)
+        packed = qmm.pack(torch.from_numpy(d["codes"]).cuda(), 4)
+        sc = torch.from_numpy(d["scales"].view(np.float16)).cuda()
+        bi = torch.from_numpy(d["biases"].view(np.float16)).cuda()
+        ids = torch.from_numpy(np.random.default_rng(0).integers(0, N, M).astype(np.int32)).cuda()
+        nbytes = M * (K // 2 + (K // 64) * 4) + M * 4 + M * K * 4
+        copies = 8
+        outs = [torch.empty((M, K), device="cuda") for _ in range(copies)]
+        calls = [(lambda i=i: qmm.gather_dequant(ids, packed, sc, bi, N, K, 4, 64, out=outs[i]))
+                 for i in range(copies)]
+    chain = Chain(calls, torch).capture(stream)
+    sec = time_graph(chain, reps, 3, torch, stream) / copies
+    gbs = nbytes / sec / 1e9
+    del chain
+    torch.cuda.empty_cache()
+    return {"kind": kind, "M": M, "N": N, "K": K, "us_per_launch": sec * 1e6, "bytes_per_launch": nbytes,
+            "gbs": gbs, "frac_of_measured_hbm": gbs / pk["hbm_gbs"], "copies": copies}
+
+
 def traffic_from_profile():
     """dram bytes per launch of the headline kernel from the committed ncu summary,
     or None if the summary is missing or the kernel source changed since."""
@@ -501,6 +557,11 @@ def main():
             try:
                 per_config[name] = measure_config(name, torch, qmm, stream, pk)
             except Exception as ex:        # report, do not hide
+                per_config[name] = {"error": repr(ex)}
+        for name in EXTRA_WORKLOADS:
+            try:
+                per_config[name] = measure_extra(name, torch, qmm, stream, pk)
+            except Exception as ex:
                 per_config[name] = {"error": repr(ex)}
 
     line = {

@@ -39,6 +39,7 @@
 #include <cudaTypedefs.h>
 
 #include "bounded_wait.cuh"
+#include "dequant_bf16.cuh"
 #include "qmm_device.cuh"
 #include "qmm_launch.h"
 #include "sm100_ptx.cuh"
@@ -87,53 +88,6 @@ struct GemmParams {
   int bn;
   int m_blocks, n_blocks, tiles;
 };
-
-// Dequantize 8 codes (one 32-bit word, k = 8c .. 8c+7) into 8 bf16 packed as
-// four 32-bit words, k order low-to-high within each word.
-//   w_j = s*q_j + b, evaluated as fma(s*16^-cls, q_j*16^cls, b): the nibble is
-//   masked in place and OR-ed into the bits of 2^23 (an exact float
-//   2^23 + q*16^cls), 2^23 is subtracted exactly, and the power-of-two
-//   pre-scaled s makes the product exact, so the FMA rounds s*q + b once.
-__device__ __forceinline__ uint4 dequant_word_bf16(uint32_t w, const f2 (&sp)[4], f2 b2) {
-  const f2 magic2 = f2_make(8388608.0f, 8388608.0f);
-  const uint32_t wh = w >> 12;
-  const uint32_t M0 = 0x4B000000u;
-  f2 q01 = f2_sub(f2_bits(and_or(w, 0xFu, M0), and_or(w, 0xF0u, M0)), magic2);
-  f2 q23 = f2_sub(f2_bits(and_or(w, 0xF00u, M0), and_or(w, 0xF000u, M0)), magic2);
-  f2 q45 = f2_sub(f2_bits(and_or(w, 0xF0000u, M0), and_or(wh, 0xF00u, M0)), magic2);
-  f2 q67 = f2_sub(f2_bits(and_or(wh, 0xF000u, M0), and_or(wh, 0xF0000u, M0)), magic2);
-  // sp[0] = (s, s/16), sp[1] = (s/256, s/4096), sp[2] = (s/65536, s/256), sp[3] = (s/4096, s/65536)
-  f2 v01 = f2_fma(q01, sp[0], b2);
-  f2 v23 = f2_fma(q23, sp[1], b2);
-  f2 v45 = f2_fma(q45, sp[2], b2);
-  f2 v67 = f2_fma(q67, sp[3], b2);
-  float a, c;
-  uint4 o;
-  f2_split(v01, a, c);
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(c), "f"(a));
-  f2_split(v23, a, c);
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(c), "f"(a));
-  f2_split(v45, a, c);
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(c), "f"(a));
-  f2_split(v67, a, c);
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(c), "f"(a));
-  return o;
-}
-
-__device__ __forceinline__ void scale_pairs(float s, f2 (&sp)[4]) {
-  const float s1 = s * 0.0625f, s2 = s * 0.00390625f, s3 = s * 0.000244140625f,
-              s4 = s * 1.52587890625e-05f;   // exact: powers of two, no underflow for binary16 s
-  sp[0] = f2_make(s, s1);
-  sp[1] = f2_make(s2, s3);
-  sp[2] = f2_make(s4, s2);
-  sp[3] = f2_make(s3, s4);
-}
-
-// Half i (0..7) of eight binary16 values held in a uint4.
-__device__ __forceinline__ uint16_t half_at(const uint4 v, int i) {
-  const uint32_t w = (i & 4) ? ((i & 2) ? v.w : v.z) : ((i & 2) ? v.y : v.x);
-  return (uint16_t)((i & 1) ? (w >> 16) : (w & 0xFFFFu));
-}
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     qmm_gemm_int4_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -235,9 +189,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           tc_fence_after();
-          const int sn = (it + 1) % STAGES;
-          const uint32_t phn = ((it + 1) / STAGES) & 1;
-          const bool fn = mbar_test(full(sn), phn), an = mbar_test(afull(sn), phn);
           const uint64_t ad = smem_desc_sw128(a_buf(s));
           const uint64_t bd = smem_desc_sw128(b_buf(s));
 #pragma unroll
@@ -246,6 +197,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
           }
           umma_commit(empty(s));          // stage free once these MMAs have read it
+          // Test the next stage only now: a test (acquire) holds back this
+          // thread's later operations until it returns (~250 cycles), which
+          // then overlaps the MMAs just issued instead of delaying them.
+          const int sn = (it + 1) % STAGES;
+          const uint32_t phn = ((it + 1) / STAGES) & 1;
+          const bool fn = mbar_test(full(sn), phn), an = mbar_test(afull(sn), phn);
           ready = fn && an;
         }
         if (!ok) break;
@@ -318,7 +275,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint2 cw = *reinterpret_cast<const uint2 *>(c_ptr(s) + t * 8);
           words[0] = cw.x, words[1] = cw.y;
         }
-        const bool next_ready = mbar_test(full((it + 1) % STAGES), ((it + 1) / STAGES) & 1);
         const uint32_t arow = a_buf(s) + r * 128;
 #pragma unroll
         for (int i = 0; i < DQ_WORDS; i++) {
@@ -331,7 +287,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(afull(s));
-        ready = __all_sync(0xffffffffu, next_ready);
+        // tested after this stage's stores, so the test's wait for its result
+        // does not hold them back
+        ready = __all_sync(0xffffffffu, mbar_test(full((it + 1) % STAGES), ((it + 1) / STAGES) & 1));
       }
     }
   } else {
@@ -353,6 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c0 = 0; c0 < bn; c0 += 32) {
         if (c0 + 32 <= bn) {
           uint32_t v[32];
+          __syncwarp();                  // tcgen05.ld is .sync.aligned: the whole warp, converged
           tmem_ld_32x32b_x32(tbase + c0, v);
           tmem_ld_wait();
           if (n < p.N) {
@@ -364,6 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         } else {
           uint32_t v[16];
+          __syncwarp();
           tmem_ld_32x32b_x16(tbase + c0, v);
           tmem_ld_wait();
           if (n < p.N) {

@@ -40,10 +40,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Non-blocking test of the same condition.  A test (or try_wait) takes about
-// 180 cycles to return even when the phase completed long ago, so a thread
-// that knows which phase it needs next issues the test early and reads the
-// result after other work.
+// Non-blocking test of the same condition.  A test (or try_wait) takes a
+// few hundred cycles to return even when the phase completed long ago, and
+// its acquire holds back the thread's later memory and tensor operations
+// until then; a thread that knows which phase it needs next issues the test
+// right after its work for the current phase and reads the result later.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
