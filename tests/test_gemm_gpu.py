@@ -24,6 +24,8 @@ SHAPES = [  # M, N, K, group: single and several tiles, ragged M and N, every BN
     (1, 128, 64, 64), (7, 200, 128, 64), (64, 256, 2048, 64), (100, 300, 1024, 128),
     (129, 1000, 512, 64), (256, 384, 2048, 64), (300, 130, 256, 64), (513, 1024, 2048, 64),
     (1024, 640, 1024, 128),
+    # more 128-row tiles than SMs: the 256-row tiling (ragged M and N, both group sizes)
+    (700, 7000, 1024, 64), (513, 5000, 512, 128),
 ]
 
 
