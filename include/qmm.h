@@ -125,9 +125,11 @@ int qmm_gemv(const float *x, const uint32_t *codes, const uint16_t *scales,
  *   the tensor cores with float32 accumulation: the fused replacement of
  *   "dequantize each weight once into an FP32 scratch buffer, then call the
  *   vendor GEMM" ("... Tesla C2075 ..." paper, section 3.1 "Prefill
- *   projections: dequantize, then call the vendor").
- *   Supported: bits 4, group in {64, 128}, K % 64 == 0, K >= 64.
- *   M == 0 or N == 0 is a no-op.
+ *   projections: dequantize, then call the vendor"), and of the Q1 page's
+ *   expand-to-FP32 prefill ("A 27B model on two 4GB Maxwell GPUs", section "A
+ *   packed Q1 prefill kernel with a narrow dispatch window").
+ *   Supported: bits 4, 8 and 1, group in {64, 128}, K % 64 == 0 (K % 128 == 0
+ *   for bits 1), K >= 64.  M == 0 or N == 0 is a no-op.
  */
 int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
              const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int bits,

@@ -101,16 +101,17 @@ int qmm_gemv(const float *x, const uint32_t *codes, const uint16_t *scales, cons
 int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
              float *y, int64_t M, int64_t N, int64_t K, int bits, int group, qmm_stream_t stream) {
   if (!bits_ok(bits) || !group_ok(group)) return QMM_ERR_UNSUPPORTED;
-  if (bits != 4 || group < 64) return QMM_ERR_UNSUPPORTED;
+  if (group < 64) return QMM_ERR_UNSUPPORTED;
   if (M < 0 || N < 0 || K < 64 || K % 64 != 0 || K % group != 0 || M >= kMaxDim || N >= kMaxDim ||
       K >= kMaxDim)
     return QMM_ERR_SHAPE;
+  if (bits == 1 && K % 128 != 0) return QMM_ERR_SHAPE;
   if (M == 0 || N == 0) return QMM_OK;
   if (!x_bf16 || !codes || !y) return QMM_ERR_ARG;
   int st = check_coeffs(scales, biases, bits);
   if (st != QMM_OK) return st;
   if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(y)) return QMM_ERR_ALIGN;
-  return cuda_status(qmm::launch_gemm(x_bf16, codes, scales, biases, y, M, N, K, group, stream));
+  return cuda_status(qmm::launch_gemm(x_bf16, codes, scales, biases, y, M, N, K, bits, group, stream));
 }
 
 size_t qmm_gemv_argmax_workspace_size(int64_t M, int64_t N) {

@@ -8,17 +8,21 @@
 // dequantization is fused into the tensor-core pipeline instead: codes travel
 // from HBM to shared memory by TMA, eight warps turn each 128-row x 64-k code
 // tile into bf16 directly in the 128-byte-swizzled K-major layout the tensor
-// core reads, and no dequantized weight ever reaches global memory.
+// core reads, and no dequantized weight ever reaches global memory.  The
+// kernel is instantiated per code format (INT4 affine, INT8 symmetric, Q1
+// signs); only the code tile width and the dequantization differ.
 //
 // Roles of one persistent CTA per SM (14 warps):
 //   warp 0      TMA producer: per K-step, the x tile (bf16, BN tokens x 64 k,
-//               128-byte swizzle) and the code tile (128 rows x 32 bytes)
+//               128-byte swizzle) and the code tile (128 rows x 32 / 64 / 16
+//               bytes for INT4 / INT8 / Q1; a Q1 chunk holds two K-steps)
 //   warp 1      TMEM allocation and the single-thread tcgen05.mma issuer
-//   warps 2-9   dequantization, two threads per weight row (32 k each):
-//               w = s*q + b in float32 (exact product, one rounding), then
-//               round-to-nearest-even bf16, stored swizzled, proxy-fenced;
-//               the row's scales and biases come eight groups at a time
-//               with 16-byte loads, one chunk ahead
+//   warps 2-9   dequantization, two threads per weight row (32 k each): the
+//               weight in float32 (INT4 s*q + b with an exact product and one
+//               rounding; INT8 s*q and Q1 +-s, exact), then round-to-nearest-
+//               even bf16, stored swizzled, proxy-fenced; the row's scales
+//               (and biases) come eight groups at a time with 16-byte loads,
+//               one chunk ahead
 //   warps 10-13 epilogue: tcgen05.ld of the f32 accumulator, y stored with
 //               32 consecutive n per warp-wide store
 //
@@ -60,15 +64,20 @@ constexpr int UMMA_K = 16;
 constexpr int DQ_WARP0 = 2, DQ_WARPS = 8, EPI_WARP0 = DQ_WARP0 + DQ_WARPS;
 constexpr int NUM_THREADS = 32 * (EPI_WARP0 + 4);
 constexpr int DQ_THREADS = 32 * DQ_WARPS;
-constexpr int DQ_TPR = DQ_THREADS / BM;            // dequantization threads per weight row
-constexpr int DQ_WORDS = (BK / 8) / DQ_TPR;        // 32-bit code words per thread per K-step
-static_assert(DQ_TPR * BM == DQ_THREADS && DQ_WORDS * DQ_TPR * 8 == BK && (DQ_WORDS == 4 || DQ_WORDS == 2),
-              "dequantization split");
+static_assert(DQ_THREADS == 2 * BM, "two dequantization threads per weight row, 32 k each");
 
+// Code bytes per weight row loaded per K-step: INT4 32, INT8 64; Q1 16 (the
+// 16-byte chunk holding 128 k, loaded for each of its two K-steps, since a
+// TMA copy cannot start inside a 16-byte unit).
+template <int BITS>
+constexpr int code_bytes_per_row() { return BITS == 4 ? 32 : BITS == 8 ? 64 : 16; }
+
+template <int BITS>
 struct Smem {
+  static constexpr int CB = code_bytes_per_row<BITS>();
   static constexpr int A_BYTES = BM * BK * 2;        // 16 KB dequantized weights (bf16)
   static constexpr int B_BYTES = BN_MAX * BK * 2;    // 32 KB x tile (bf16), BN rows used
-  static constexpr int C_BYTES = BM * BK / 2;        // 4 KB codes
+  static constexpr int C_BYTES = BM * CB;            // codes: 4 KB (INT4), 8 KB (INT8), 2 KB (Q1)
   static constexpr int STAGE = A_BYTES + B_BYTES + C_BYTES;
   static constexpr int BAR_OFF = STAGES * STAGE;     // multiple of 1024
   static constexpr int BARS = 3 * STAGES + 4 + 1;    // full, afull, empty, acc_full[2], acc_empty[2], drain
@@ -89,10 +98,11 @@ struct GemmParams {
   int m_blocks, n_blocks, tiles;
 };
 
+template <int BITS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    qmm_gemm_int4_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                         const __grid_constant__ CUtensorMap tmap_codes, const GemmParams p) {
-  using S = Smem;
+    qmm_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                    const __grid_constant__ CUtensorMap tmap_codes, const GemmParams p) {
+  using S = Smem<BITS>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // align the working area to 1024 bytes (128-byte swizzle atoms)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -153,7 +163,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(full(s), tx);
           tma_load_2d(b_buf(s), &tmap_x, kb * BK, mb * bn, full(s));
-          tma_load_2d(c_buf(s), &tmap_codes, kb * (BK / 2), nb * BM, full(s));
+          const int cx = BITS == 1 ? (kb >> 1) * S::CB : kb * S::CB;   // byte column of the code chunk
+          tma_load_2d(c_buf(s), &tmap_codes, cx, nb * BM, full(s));
         }
       }
       if (!ok) {
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp < EPI_WARP0) {
     // ------------------------------------------------------------ dequantization
     const int t = threadIdx.x - DQ_WARP0 * 32;      // 0 .. DQ_THREADS - 1
-    const int r = t / DQ_TPR, part = t % DQ_TPR;    // weight row within the tile, k part
+    const int r = t >> 1, part = t & 1;             // weight row within the tile, k half
     const int G = p.groups_per_row;
     int it = 0;
     bool ok = true;
@@ -226,16 +237,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = nb * BM + r;
       const bool row_ok = row < p.N;
       const uint16_t *srow = p.scales + (int64_t)(row_ok ? row : 0) * G;
-      const uint16_t *brow = p.biases + (int64_t)(row_ok ? row : 0) * G;
+      const uint16_t *brow = BITS == 4 ? p.biases + (int64_t)(row_ok ? row : 0) * G : nullptr;
       // coefficients: eight groups per 16-byte load, current and next chunk
       uint4 sc_cur = make_uint4(0, 0, 0, 0), bc_cur = sc_cur, sc_nxt = sc_cur, bc_nxt = sc_cur;
       int cur_chunk = 0;
       if (p.coef_vec && row_ok) {
         sc_cur = ld_stream_u4(srow);
-        bc_cur = ld_stream_u4(brow);
+        if (BITS == 4) bc_cur = ld_stream_u4(brow);
         if (G > 8) {
           sc_nxt = ld_stream_u4(srow + 8);
-          bc_nxt = ld_stream_u4(brow + 8);
+          if (BITS == 4) bc_nxt = ld_stream_u4(brow + 8);
         }
       }
       for (int kb = 0; kb < ksteps; kb++, it++) {
@@ -251,35 +262,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               bc_cur = bc_nxt;
               if ((cur_chunk + 1) * 8 < G) {
                 sc_nxt = ld_stream_u4(srow + (cur_chunk + 1) * 8);
-                bc_nxt = ld_stream_u4(brow + (cur_chunk + 1) * 8);
+                if (BITS == 4) bc_nxt = ld_stream_u4(brow + (cur_chunk + 1) * 8);
               }
             }
             sb = half_at(sc_cur, g & 7);
-            bb = half_at(bc_cur, g & 7);
+            if (BITS == 4) bb = half_at(bc_cur, g & 7);
           } else {
             sb = ld_nc_u16(srow + g);
-            bb = ld_nc_u16(brow + g);
+            if (BITS == 4) bb = ld_nc_u16(brow + g);
           }
         }
         const float sf = row_ok ? h2f(sb) : 0.0f;
         const float bf = row_ok ? h2f(bb) : 0.0f;
-        f2 sp[4];
-        scale_pairs(sf, sp);
-        const f2 b2 = f2_make(bf, bf);
-        if (!ready && !__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
-        uint32_t words[DQ_WORDS];                                          // 8 * DQ_WORDS codes of row r
-        if constexpr (DQ_WORDS == 4) {
-          const uint4 cw = *reinterpret_cast<const uint4 *>(c_ptr(s) + t * 16);
-          words[0] = cw.x, words[1] = cw.y, words[2] = cw.z, words[3] = cw.w;
+        f2 sp[4], b2, s2;
+        uint32_t sbf = 0;
+        if constexpr (BITS == 4) {
+          scale_pairs(sf, sp);
+          b2 = f2_make(bf, bf);
+        } else if constexpr (BITS == 8) {
+          s2 = f2_make(sf, sf);
         } else {
-          const uint2 cw = *reinterpret_cast<const uint2 *>(c_ptr(s) + t * 8);
-          words[0] = cw.x, words[1] = cw.y;
+          sbf = bf16_pair(sf);
         }
+        if (!ready && !__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
+        // this thread's 32 k of row r (k = 32 * part ..)
+        uint32_t words[8];
+        if constexpr (BITS == 4) {
+          const uint4 cw = *reinterpret_cast<const uint4 *>(c_ptr(s) + r * 32 + part * 16);
+          words[0] = cw.x, words[1] = cw.y, words[2] = cw.z, words[3] = cw.w;
+        } else if constexpr (BITS == 8) {
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(c_ptr(s) + r * 64 + part * 32);
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(c_ptr(s) + r * 64 + part * 32 + 16);
+          words[0] = c0.x, words[1] = c0.y, words[2] = c0.z, words[3] = c0.w;
+          words[4] = c1.x, words[5] = c1.y, words[6] = c1.z, words[7] = c1.w;
+        } else {
+          words[0] = *reinterpret_cast<const uint32_t *>(c_ptr(s) + r * 16 + (kb & 1) * 8 + part * 4);
+        }
+        // the next stage's readiness, tested early: its result is read after
+        // this stage's stores (measured faster than testing after them)
+        const bool next_ready = mbar_test(full((it + 1) % STAGES), ((it + 1) / STAGES) & 1);
         const uint32_t arow = a_buf(s) + r * 128;
 #pragma unroll
-        for (int i = 0; i < DQ_WORDS; i++) {
-          const int c = DQ_WORDS * part + i;                               // 16-byte chunk: k = 8c..8c+7
-          const uint4 v = dequant_word_bf16(words[i], sp, b2);
+        for (int i = 0; i < 4; i++) {
+          const int c = 4 * part + i;                                      // 16-byte chunk: k = 8c..8c+7
+          uint4 v;
+          if constexpr (BITS == 4) v = dequant_word_bf16(words[i], sp, b2);
+          else if constexpr (BITS == 8) v = dequant_int8x8_bf16(words[2 * i], words[2 * i + 1], s2);
+          else v = signs8_bf16(words[0] >> (8 * i), sbf);
           const uint32_t dst = arow + ((c ^ (r & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
                        "r"(v.w)
@@ -287,9 +316,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(afull(s));
-        // tested after this stage's stores, so the test's wait for its result
-        // does not hold them back
-        ready = __all_sync(0xffffffffu, mbar_test(full((it + 1) % STAGES), ((it + 1) / STAGES) & 1));
+        ready = __all_sync(0xffffffffu, next_ready);
       }
     }
   } else {
@@ -398,25 +425,12 @@ int pick_bn(int64_t M, int64_t N, int sms) {
 
 }  // namespace
 
-cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
-                        const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int group,
-                        cudaStream_t s) {
-  using S = Smem;
-  GemmParams p{};
-  p.scales = scales;
-  p.biases = biases;
-  p.y = y;
-  p.M = (int)M;
-  p.N = (int)N;
-  p.K = (int)K;
-  p.gshift = __builtin_ctz((unsigned)group);
-  p.groups_per_row = (int)(K / group);
-  p.coef_vec = (p.groups_per_row % 8 == 0) ? 1 : 0;   // rows are then 16-byte multiples (bases are 16-aligned)
-  p.bn = pick_bn(M, N, sm_count_gemm());
-  p.m_blocks = (int)((M + p.bn - 1) / p.bn);
-  p.n_blocks = (int)((N + BM - 1) / BM);
-  p.tiles = p.m_blocks * p.n_blocks;
+namespace {
 
+template <int BITS>
+cudaError_t launch_bits(const uint16_t *x_bf16, const uint32_t *codes, const GemmParams &p, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t s) {
+  using S = Smem<BITS>;
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap tx, tc;
@@ -431,21 +445,47 @@ cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uin
       return cudaErrorInvalidValue;
   }
   {
-    cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
-    cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-    cuuint32_t box[2] = {BK / 2, BM};
+    // codes as bytes: [N, K*BITS/8], box of CB bytes x 128 rows
+    cuuint64_t dims[2] = {(cuuint64_t)(K * BITS / 8), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(K * BITS / 8)};
+    cuuint32_t box[2] = {(cuuint32_t)S::CB, BM};
     cuuint32_t es[2] = {1, 1};
     if (encode(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t *>(codes), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kern = qmm_gemm_int4_kernel;
+  auto kern = qmm_gemm_kernel<BITS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
   if (e != cudaSuccess) return e;
   const int grid = p.tiles < sm_count_gemm() ? p.tiles : sm_count_gemm();
   kern<<<grid, NUM_THREADS, S::ALLOC, s>>>(tx, tc, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
+                        const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int bits, int group,
+                        cudaStream_t s) {
+  GemmParams p{};
+  p.scales = scales;
+  p.biases = biases;
+  p.y = y;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.gshift = __builtin_ctz((unsigned)group);
+  p.groups_per_row = (int)(K / group);
+  p.coef_vec = (p.groups_per_row % 8 == 0) ? 1 : 0;   // rows are then 16-byte multiples (bases are 16-aligned)
+  p.bn = pick_bn(M, N, sm_count_gemm());
+  p.m_blocks = (int)((M + p.bn - 1) / p.bn);
+  p.n_blocks = (int)((N + BM - 1) / BM);
+  p.tiles = p.m_blocks * p.n_blocks;
+  if (bits == 4) return launch_bits<4>(x_bf16, codes, p, M, N, K, s);
+  if (bits == 8) return launch_bits<8>(x_bf16, codes, p, M, N, K, s);
+  if (bits == 1) return launch_bits<1>(x_bf16, codes, p, M, N, K, s);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t read_clear_gemm_status(int *status, cudaStream_t s) {

@@ -65,9 +65,10 @@ cudaError_t launch_gemv_batch(const float *x, const uint32_t *codes, const uint1
                               const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits,
                               int group, cudaStream_t s);
 
-// Prefill product, bits == 4, group in {64, 128}, K % 64 == 0, M >= 1, N >= 1.
+// Prefill product, bits in {1, 4, 8}, group in {64, 128}, K % 64 == 0 (K % 128
+// for bits 1), M >= 1, N >= 1.
 cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
-                        const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K,
+                        const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int bits,
                         int group, cudaStream_t s);
 
 // Device status words written by kernels whose bounded waits ran out (one per

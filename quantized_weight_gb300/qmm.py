@@ -167,7 +167,7 @@ def gemv(x, packed, scales, biases, N, bits, group, out=None, stream=None) -> to
 
 
 def gemm(x, packed, scales, biases, N, bits, group, out=None, stream=None) -> torch.Tensor:
-    """Prefill product y[M, N] = x[M, K] . dequant(W)^T, bfloat16 x, any M."""
+    """Prefill product y[M, N] = x[M, K] . dequant(W)^T, bfloat16 x, any M, bits 4 / 8 / 1."""
     M, K = x.shape
     _need(x, "x", torch.bfloat16)
     _need(packed, "packed", torch.int32, (N, K * bits // 32))

@@ -66,7 +66,9 @@ def test_gemv_validation(L):
 
 
 def test_gemm_validation(L):
-    assert gemm(L, bits=8, b=None) == UNSUP        # prefill: INT4 only
+    assert gemm(L, bits=2, b=None) == UNSUP
+    assert gemm(L, bits=8, b=FAKE) == ARG          # INT8 takes no biases
+    assert gemm(L, bits=1, b=None, K=192) == SHAPE  # Q1 prefill needs K % 128
     assert gemm(L, g=32) == UNSUP
     assert gemm(L, K=32) == SHAPE
     assert gemm(L, K=96) == SHAPE

@@ -43,6 +43,27 @@ def test_small_shapes(qmm, oracle_mod, M, N, K, group):
     assert err <= TOL, (M, N, K, group, err)
 
 
+FORMATS = [  # M, N, K, bits, group: INT8 and Q1 codes through the same tensor-core pipeline
+    (1, 128, 128, 8, 64), (100, 300, 1024, 8, 128), (513, 1024, 2048, 8, 64), (700, 7000, 1024, 8, 64),
+    (1, 128, 128, 1, 128), (129, 1000, 512, 1, 64), (300, 130, 256, 1, 128), (1024, 2048, 5120, 1, 128),
+]
+
+
+@pytest.mark.parametrize("M,N,K,bits,group", FORMATS)
+def test_int8_and_q1_prefill(qmm, oracle_mod, M, N, K, bits, group):
+    d = inputs.make(M, N, K, bits, group, seed=M + N + K + bits, prefill=True)
+    t = to_device(d, bits, with_bf16=True)
+    p = qmm.pack(t["codes"], bits)
+    y = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], N, bits, group)
+    qmm.check()
+    y = y.cpu().numpy()
+    ref = oracle_mod.qmm_bf16x(d["x_bf16"], oracle_mod.pack(d["codes"], bits), d["scales"], d["biases"],
+                              N, K, bits, group)
+    assert rel_l2_rows(y, ref) <= TOL, (M, N, K, bits, group)
+    y2 = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], N, bits, group).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
 @pytest.mark.parametrize("name", ["prefill_int4_m1024_k2048_n6144", "prefill_int4_m256_k2048_n151936"])
 def test_full_size_sampled(qmm, oracle_mod, name):
     w = inputs.WORKLOADS[name]
