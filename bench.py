@@ -220,11 +220,11 @@ def measure_config(name, torch, qmm, stream, pk, reps=20):
     """Per-launch time of one workload with L2-cold weights (copies > L2)."""
     w, d, t = device_inputs(name, 0, torch, qmm)
     if w.prefill:
-        per = w.N * w.K // 2 + w.M * w.K * 2 + w.N * (w.K // w.group) * 4
+        per = w.N * w.K * w.bits // 8 + w.M * w.K * 2 + w.N * (w.K // w.group) * (4 if w.bits == 4 else 2)
     else:
         per = gemv_bytes(w.M, w.N, w.K, w.bits, w.group)
     copies = max(2, min(64, -(-4 * l2_bytes(torch) // per)))
-    if w.prefill and w.N * w.K // 2 > l2_bytes(torch):
+    if w.prefill and w.N * w.K * w.bits // 8 > l2_bytes(torch):
         copies = 2
     ts = replicate(t, copies, torch)
     ys = [torch.empty((w.M, w.N), dtype=torch.float32, device="cuda") for _ in range(copies)]

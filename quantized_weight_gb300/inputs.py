@@ -56,6 +56,10 @@ WORKLOADS = {w.name: w for w in [
              note="prefill at the MLP up-projection shape"),
     Workload("prefill_int4_m256_k2048_n151936", 256, 2048, 151936, 4, 64, prefill=True,
              note="prefill through a tied output head"),
+    Workload("prefill_int8_m1024_k2048_n6144", 1024, 2048, 6144, 8, 64, prefill=True,
+             note="8-bit prefill at the MLP up-projection shape"),
+    Workload("prefill_q1_m1024_k5120_n17408", 1024, 5120, 17408, 1, 128, prefill=True,
+             note="binary Q1 prefill at the 27B-class FFN shape"),
 ]}
 
 SCALE_RANGE = {4: (0.001, 0.02), 8: (1e-4, 5e-3), 1: (0.005, 0.05)}

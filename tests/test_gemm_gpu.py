@@ -64,24 +64,25 @@ def test_int8_and_q1_prefill(qmm, oracle_mod, M, N, K, bits, group):
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
-@pytest.mark.parametrize("name", ["prefill_int4_m1024_k2048_n6144", "prefill_int4_m256_k2048_n151936"])
+@pytest.mark.parametrize("name", ["prefill_int4_m1024_k2048_n6144", "prefill_int4_m256_k2048_n151936",
+                                  "prefill_int8_m1024_k2048_n6144", "prefill_q1_m1024_k5120_n17408"])
 def test_full_size_sampled(qmm, oracle_mod, name):
     w = inputs.WORKLOADS[name]
     d = inputs.make_workload(name)
-    t = to_device(d, 4, with_bf16=True)
-    p = qmm.pack(t["codes"], 4)
-    y = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, 4, w.group)
+    t = to_device(d, w.bits, with_bf16=True)
+    p = qmm.pack(t["codes"], w.bits)
+    y = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, w.bits, w.group)
     qmm.check()
     rng = np.random.default_rng(123)
     rows = rng.choice(w.M, size=min(48, w.M), replace=False)
     cols = np.concatenate([rng.choice(w.N, size=60, replace=False), [0, w.N - 1]])
     ms, ns = np.repeat(rows, cols.size), np.tile(cols, rows.size)
-    ref = oracle_mod.qmm_sampled(d["x_bf16"], oracle_mod.pack(d["codes"], 4), d["scales"], d["biases"],
-                                 ms, ns, w.N, w.K, 4, w.group).reshape(rows.size, cols.size)
+    ref = oracle_mod.qmm_sampled(d["x_bf16"], oracle_mod.pack(d["codes"], w.bits), d["scales"], d["biases"],
+                                 ms, ns, w.N, w.K, w.bits, w.group).reshape(rows.size, cols.size)
     got = y[torch_index(rows), :][:, torch_index(cols)].cpu().numpy()
     # relative L2 over the sampled entries of each row estimates the row's relative L2
     assert rel_l2_rows(got, ref) <= TOL
-    y2 = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, 4, w.group)
+    y2 = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, w.bits, w.group)
     import torch
     assert torch.equal(y, y2)                    # same bits on every run
 
