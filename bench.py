@@ -295,7 +295,7 @@ def measure_extra(name, torch, qmm, stream, pk, reps=20):
     chain = Chain(calls, torch).capture(stream)
     sec = time_graph(chain, reps, 3, torch, stream) / copies
     gbs = nbytes / sec / 1e9
-    del chain
+    del chain, e2e_chain
     torch.cuda.empty_cache()
     return {"kind": kind, "M": M, "N": N, "K": K, "us_per_launch": sec * 1e6, "bytes_per_launch": nbytes,
             "gbs": gbs, "frac_of_measured_hbm": gbs / pk["hbm_gbs"], "copies": copies}
@@ -515,22 +515,31 @@ def main():
     per_launch_s = sec / args.steps / launches_per_step
     achieved = (step_bytes / launches_per_step) / per_launch_s / 1e9
 
-    # ---- end to end through the public API: host activations in, host results out
-    xs_h = [torch.empty_like(t["x"], device="cpu").pin_memory() for t in ups + dns]
-    for h, t in zip(xs_h, ups + dns):
-        h.copy_(t["x"].cpu())
-    ys_h = [torch.empty_like(y, device="cpu").pin_memory() for y in y_up + y_dn]
-    xs_d = [t["x"] for t in ups + dns]
-    ys_d = y_up + y_dn
-    h2d = sum(h.numel() * 4 for h in xs_h)
-    d2h = sum(h.numel() * 4 for h in ys_h)
+    # ---- end to end through the public API: host activations in, host results out.
+    # Every step copies all layers' activations from pinned host memory in one
+    # copy per projection, runs the 2L products (qmm.gemv calls captured once in
+    # a CUDA graph, as a decode loop runs them) and reads all results back.
+    X_up = torch.stack([t["x"][0] for t in ups])          # [L, K_up]
+    X_dn = torch.stack([t["x"][0] for t in dns])          # [L, K_dn]
+    Y_up = torch.empty((layers, up_w.N), device="cuda")
+    Y_dn = torch.empty((layers, dn_w.N), device="cuda")
+    X_up_h, X_dn_h = X_up.cpu().pin_memory(), X_dn.cpu().pin_memory()
+    Y_up_h = torch.empty(Y_up.shape, dtype=torch.float32).pin_memory()
+    Y_dn_h = torch.empty(Y_dn.shape, dtype=torch.float32).pin_memory()
+    e2e_calls = []
+    for i in range(layers):
+        e2e_calls.append(gemv_call(qmm, dict(ups[i], x=X_up[i:i + 1]), up_w, Y_up[i:i + 1]))
+        e2e_calls.append(gemv_call(qmm, dict(dns[i], x=X_dn[i:i + 1]), dn_w, Y_dn[i:i + 1]))
+    e2e_chain = Chain(e2e_calls, torch).capture(stream)
+    h2d = (X_up_h.numel() + X_dn_h.numel()) * 4
+    d2h = (Y_up_h.numel() + Y_dn_h.numel()) * 4
 
     def e2e_step():
-        for h, dtens in zip(xs_h, xs_d):
-            dtens.copy_(h, non_blocking=True)
-        chain.launch_eager()
-        for h, dtens in zip(ys_h, ys_d):
-            h.copy_(dtens, non_blocking=True)
+        X_up.copy_(X_up_h, non_blocking=True)
+        X_dn.copy_(X_dn_h, non_blocking=True)
+        e2e_chain.graph.replay()
+        Y_up_h.copy_(Y_up, non_blocking=True)
+        Y_dn_h.copy_(Y_dn, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     with torch.cuda.stream(stream):
@@ -545,10 +554,13 @@ def main():
         f1.record(stream)
         f1.synchronize()
         barrier()
+    # the results read back are the products of the copied activations
+    e2e_ok = bool(torch.equal(Y_up_h[0].cuda(), qmm.gemv(X_up[0:1], ups[0]["packed"], ups[0]["scales"],
+                                                         ups[0]["biases"], up_w.N, 4, 64)[0]))
     e2e_sec = slowest_rank_seconds(f0.elapsed_time(f1) / 1000.0, world, "cuda")
     e2e_val = job_gbs(step_bytes, e2e_steps, world, e2e_sec)
 
-    del chain
+    del chain, e2e_chain
     torch.cuda.empty_cache()
 
     per_config = {}
@@ -581,8 +593,9 @@ def main():
                      "kernel": "gemv_stream_kernel<4> (INT4 decode product)",
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps,
-                "path": "pinned host x -> device, per-product Python API calls, device y -> pinned host"},
+                "steps": e2e_steps, "results_checked": e2e_ok,
+                "path": "pinned host x -> device (one copy per projection), the 2L qmm.gemv calls replayed "
+                        "from a CUDA graph, device y -> pinned host (one copy per projection)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "per_config": per_config,
