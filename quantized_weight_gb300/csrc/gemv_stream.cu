@@ -19,7 +19,8 @@
 // A warp takes every wps-th group of 4 rows of the slab; per group the lanes
 // form partial dot products with exact bit tricks (below), a transposing
 // butterfly reduces the 4 rows over the warp (6 shuffles), and the totals go to
-// a per-row, per-segment slot in shared memory.  When every warp is done, one
+// a per-row, per-segment slot in shared memory.  When every warp is done (a
+// named barrier among the consumer warps), one
 // thread per row adds the segment slots in segment order and stores y: no
 // atomics, the same bits on every run.
 //
@@ -189,7 +190,6 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
   auto full = [&](int s) { return bars + 8 * s; };
   auto empty = [&](int s) { return bars + 8 * (S + s); };
   const uint32_t coef_full = bars + 8 * (2 * S);
-  const uint32_t done_bar = bars + 8 * (2 * S + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_bar + 8 * (2 * S + 2));
   const WaitCtl ctl{abort_flag, &g_gemv_status};
 
@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
       mbar_init(empty(s), groups_per_stage * p.segs);   // one arrival per (group, segment)
     }
     mbar_init(coef_full, 1);
-    mbar_init(done_bar, consumers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -340,10 +339,11 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
     const int rr = (h16 ? 2 : 0) + (h8 ? 1 : 0);
     if ((lane & 7) == 0 && rr < nr) red[(rbase + rr) * p.segs + seg] = k;
   }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(done_bar);
-  // one thread per row adds the segment totals in segment order
-  const bool fin = ok && __all_sync(0xffffffffu, wait_bounded(done_bar, 0, ctl));
+  // every consumer warp gets here (the loop above only ends or breaks), so
+  // the named barrier completes; after it, one thread per row adds the
+  // segment totals in segment order, unless some wait of the CTA ran out
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  const bool fin = ok && !*abort_flag;
   if constexpr (ARGMAX) {
     // every consumer warp takes part, also after an abort (with no candidate),
     // so the CTA barrier inside completes and the CTA is counted
