@@ -52,6 +52,7 @@ constexpr uint32_t kMagic = 0x4B000000u;   // bit pattern of 2^23
 constexpr int RG = 4;                      // rows per group (one butterfly)
 constexpr int STAGE_ROWS_MAX = 16;         // rows per code stage
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemPair = 108 * 1024;      // leaves room for two CTAs per SM
 constexpr int kMaxConsumerWarps = 15;
 
 template <int BITS>
@@ -76,6 +77,7 @@ struct StreamParams {
   int stage_rows;      // rows per code stage (multiple of RG)
   int stages;          // ring depth
   int rows_per_cta;
+  int two_per_sm;      // two CTAs fit on an SM (so the next product's copies start early)
   // shared-memory layout (bytes from the 128-byte-aligned base)
   int off_coef, off_x, off_red, off_bar, off_am;
   ArgmaxWork am;       // used by the argmax epilogue only
@@ -175,6 +177,37 @@ __device__ __forceinline__ int pair_of(int j, int &slot) {
 
 // ARGMAX: instead of storing y, the epilogue reduces this CTA's rows to their
 // greedy argmax and the last CTA combines the CTAs' winners (argmax.cuh).
+// Stages x (K floats) into shared memory as each lane's register pairs:
+// coalesced float4 loads, XU of them in flight per thread before its stores.
+template <int BITS, int XU>
+__device__ __forceinline__ void stage_x(const float *__restrict__ x, int K, f2 *xs, int ct, int nthreads) {
+  using L = Lane<BITS>;
+  const int units = K / 4;
+  for (int u0 = ct; u0 < units; u0 += XU * nthreads) {
+    float4 v[XU];
+#pragma unroll
+    for (int i = 0; i < XU; i++) {
+      const int u = u0 + i * nthreads;
+      v[i] = u < units ? ld_nc_f4(x + 4 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < XU; i++) {
+      const int u = u0 + i * nthreads;
+      if (u >= units) break;
+      const int k = 4 * u;
+      const int sg = k / L::SEG_W, l = (k % L::SEG_W) / L::W, jj = k % L::W;
+      const float vv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        int slot;
+        const int pi = pair_of<BITS>(jj + e, slot);
+        float *dst = reinterpret_cast<float *>(&xs[(sg * L::PAIRS + pi) * 32 + l]);
+        dst[slot] = vv[e];
+      }
+    }
+  }
+}
+
 template <int BITS, bool ARGMAX>
 __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams p) {
   using L = Lane<BITS>;
@@ -250,27 +283,36 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
   const int cw = warp - 1;
   const int ct = cw * 32 + lane;                                // consumer thread index
   const int nthreads = consumers * 32;
+  const int seg = cw % p.segs, t0 = cw / p.segs;
+  const int ngroups = (rows + RG - 1) / RG;
+  // The coefficients and the first S stages of codes (first use of every
+  // ring slot) do not depend on the previous kernel: wait for them before the
+  // dependent-launch wait, where the waits' latency (a few hundred ns each,
+  // even for copies that landed long ago) overlaps the previous product's tail.
+  // This pays only when two CTAs share an SM: this CTA's copies were then
+  // issued while the previous product ran.  With one CTA per SM the copies
+  // start with this kernel, and the x staging below overlaps their transfer.
+  bool ok = true;
+  int prewaited = -1;                                            // stages < S waited for already
+  if (p.two_per_sm) {
+    ok = __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
+    for (int grp = t0; ok && grp < ngroups; grp += p.wps) {
+      const int j = grp / groups_per_stage;
+      if (j >= S) break;
+      if (j > prewaited) {
+        if (!__all_sync(0xffffffffu, wait_bounded(full(j), 0, ctl))) ok = false;
+        prewaited = j;
+      }
+    }
+  }
   pdl_wait();                                                    // x is written by the previous kernel
   {
     // x, once per CTA, coalesced; stored as each lane's register pairs
-    const int units = p.K / 4;
-    for (int u = ct; u < units; u += nthreads) {
-      const float4 v = ld_nc_f4(p.x + 4 * u);
-      const int k = 4 * u;
-      const int sg = k / L::SEG_W, l = (k % L::SEG_W) / L::W, j = k % L::W;
-      const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        int slot;
-        const int pi = pair_of<BITS>(j + e, slot);
-        float *dst = reinterpret_cast<float *>(&xs[(sg * L::PAIRS + pi) * 32 + l]);
-        dst[slot] = vv[e];
-      }
-    }
+    if (p.two_per_sm) stage_x<BITS, 4>(p.x, p.K, xs, ct, nthreads);
+    else stage_x<BITS, 1>(p.x, p.K, xs, ct, nthreads);
     // consumer warps only; every consumer thread reaches it (no exit before)
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
   }
-  const int seg = cw % p.segs, t0 = cw / p.segs;
   f2 xp[L::PAIRS];
 #pragma unroll
   for (int i = 0; i < L::PAIRS; i++) xp[i] = xs[(seg * L::PAIRS + i) * 32 + lane];
@@ -285,14 +327,13 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
   }
   const int g = (seg * L::SEG_W + lane * L::W) >> p.gshift;    // a lane chunk lies in one group
   const int lane_off = seg * L::SEG_BYTES + lane * L::BYTES;
-  bool ok = __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
+  if (!p.two_per_sm) ok = __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
 
-  const int ngroups = (rows + RG - 1) / RG;
   for (int grp = t0; ok && grp < ngroups; grp += p.wps) {
     const int j = grp / groups_per_stage;                        // stage holding this group
     const int s = j % S;
     const uint32_t ph = (j / S) & 1;
-    if (!__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
+    if (j > prewaited && !__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
     const int rbase = grp * RG;                                  // first row (within the CTA)
     const int nr = min(RG, rows - rbase);
     const uint8_t *st = smem + s * code_stage_bytes + (rbase - j * p.stage_rows) * p.row_bytes;
@@ -394,17 +435,30 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   grid = (int)((N + RG - 1) / RG);
   if (grid > sm_count_stream()) grid = sm_count_stream();
   p.rows_per_cta = (int)((N + grid - 1) / grid);            // the largest slab of the even split
-  p.stage_rows = STAGE_ROWS_MAX;
-  while (p.stage_rows > RG && p.stage_rows / 2 >= p.rows_per_cta) p.stage_rows /= 2;
-  const int nst = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
   const int coef = p.rows_per_cta * G * 2 * (BITS == 4 ? 2 : 1);
   const int xbytes = (int)K * 4;
   const int redb = p.rows_per_cta * p.segs * 4;
   const int fixed = coef + xbytes + redb + 8 * 64;
-  const int stage_bytes = p.stage_rows * p.row_bytes;
-  int S = (kSmemBudget - fixed) / stage_bytes;
-  if (S > nst) S = nst;
+  int stage_rows0 = STAGE_ROWS_MAX;
+  while (stage_rows0 > RG && stage_rows0 / 2 >= p.rows_per_cta) stage_rows0 /= 2;
+  // Prefer a ring small enough for two CTAs per SM (the next product's CTA
+  // then starts, and its first copies land, while this one still runs), as
+  // long as it keeps two stages in flight; else the deepest ring that fits.
+  int S = 0;
+  for (int sr = stage_rows0; sr >= RG && S == 0; sr /= 2) {
+    const int nst = (p.rows_per_cta + sr - 1) / sr;
+    int s2 = (kSmemPair - fixed) / (sr * p.row_bytes);
+    if (s2 > nst) s2 = nst;
+    if (s2 >= 2 || s2 == nst) S = s2, p.stage_rows = sr;
+  }
+  if (S < 1) {
+    p.stage_rows = stage_rows0;
+    const int nst = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
+    S = (kSmemBudget - fixed) / (p.stage_rows * p.row_bytes);
+    if (S > nst) S = nst;
+  }
   if (S < 1) return false;
+  const int stage_bytes = p.stage_rows * p.row_bytes;
   p.stages = S;
   p.off_coef = S * stage_bytes;
   p.off_x = (p.off_coef + coef + 15) & ~15;
@@ -412,6 +466,7 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   p.off_bar = (p.off_red + redb + 7) & ~7;
   p.off_am = (p.off_bar + 8 * (2 * S + 2) + 16 + 15) & ~15;
   smem = (size_t)p.off_am + 8 * 16;
+  p.two_per_sm = 2 * (smem + 1024) <= 228 * 1024 ? 1 : 0;   // 1 KB reserved per CTA
   int wps = kMaxConsumerWarps / p.segs;
   const int ngroups = (p.rows_per_cta + RG - 1) / RG;
   if (wps > ngroups) wps = ngroups;
