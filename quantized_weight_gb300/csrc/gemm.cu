@@ -59,7 +59,8 @@ using namespace sm100;
 constexpr int BM = 128;                // weight rows per tile (MMA M)
 constexpr int BK = 64;                 // k per stage: one 128-byte swizzle atom of bf16
 constexpr int BN_MAX = 256;            // tokens per tile (MMA N), at most
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 8;           // ring depth: as many stages as shared memory holds
+constexpr int SMEM_LIMIT = 227 * 1024;    // dynamic shared memory per CTA
 constexpr int UMMA_K = 16;
 constexpr int DQ_WARP0 = 2, DQ_WARPS = 8, EPI_WARP0 = DQ_WARP0 + DQ_WARPS;
 constexpr int NUM_THREADS = 32 * (EPI_WARP0 + 4);
@@ -72,18 +73,33 @@ static_assert(DQ_THREADS == 2 * BM, "two dequantization threads per weight row, 
 template <int BITS>
 constexpr int code_bytes_per_row() { return BITS == 4 ? 32 : BITS == 8 ? 64 : 16; }
 
+// One ring stage: the dequantized weight tile, the x tile (BN rows of 128
+// bytes) and the code tile, each a multiple of 1024 bytes (swizzle atoms).
+// The stage size depends on BN, so the ring depth is chosen per call.
 template <int BITS>
 struct Smem {
   static constexpr int CB = code_bytes_per_row<BITS>();
   static constexpr int A_BYTES = BM * BK * 2;        // 16 KB dequantized weights (bf16)
-  static constexpr int B_BYTES = BN_MAX * BK * 2;    // 32 KB x tile (bf16), BN rows used
   static constexpr int C_BYTES = BM * CB;            // codes: 4 KB (INT4), 8 KB (INT8), 2 KB (Q1)
-  static constexpr int STAGE = A_BYTES + B_BYTES + C_BYTES;
-  static constexpr int BAR_OFF = STAGES * STAGE;     // multiple of 1024
-  static constexpr int BARS = 3 * STAGES + 4 + 1;    // full, afull, empty, acc_full[2], acc_empty[2], drain
-  static constexpr int TOTAL = BAR_OFF + BARS * 8 + 16 /* tmem slot + abort flag */;
-  static constexpr int ALLOC = TOTAL + 1024;         // slack to align the base to 1024
+  static constexpr int BARS = 3 * MAX_STAGES + 4 + 1;  // full, afull, empty, acc_full[2], acc_empty[2], drain
+  static constexpr int TAIL = BARS * 8 + 16 /* tmem slot + abort flag */ + 1024 /* base alignment slack */;
   static constexpr uint32_t TMEM_COLS = 2 * BN_MAX;  // two accumulators
+  static constexpr int stage_bytes(int bn) { return A_BYTES + bn * BK * 2 + C_BYTES; }
+  static constexpr int stages(int bn) {
+    const int n = (SMEM_LIMIT - TAIL) / stage_bytes(bn);
+    return n > MAX_STAGES ? MAX_STAGES : n;
+  }
+  static constexpr int alloc(int bn) { return stages(bn) * stage_bytes(bn) + TAIL; }
+};
+
+// Position in the stage ring: slot and phase parity, advanced without a
+// division (the ring depth is a runtime value).
+struct Ring {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int stages) {
+    if (++s == stages) s = 0, ph ^= 1u;
+  }
 };
 
 struct GemmParams {
@@ -95,6 +111,7 @@ struct GemmParams {
   int groups_per_row;
   int coef_vec;          // coefficient rows load as 16-byte vectors
   int bn;
+  int stages;            // ring depth
   int m_blocks, n_blocks, tiles;
 };
 
@@ -108,19 +125,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
-  auto a_buf = [&](int s) { return sbase + s * S::STAGE; };
-  auto b_buf = [&](int s) { return sbase + s * S::STAGE + S::A_BYTES; };
-  auto c_ptr = [&](int s) { return smem + s * S::STAGE + S::A_BYTES + S::B_BYTES; };
-  auto c_buf = [&](int s) { return sbase + s * S::STAGE + S::A_BYTES + S::B_BYTES; };
-  const uint32_t bars = sbase + S::BAR_OFF;
+  const int STAGES = p.stages;
+  const int stage_bytes = S::stage_bytes(p.bn);
+  const int b_off = S::A_BYTES, c_off = S::A_BYTES + p.bn * BK * 2;
+  auto a_buf = [&](int s) { return sbase + s * stage_bytes; };
+  auto b_buf = [&](int s) { return sbase + s * stage_bytes + b_off; };
+  auto c_ptr = [&](int s) { return smem + s * stage_bytes + c_off; };
+  auto c_buf = [&](int s) { return sbase + s * stage_bytes + c_off; };
+  const int bar_off = STAGES * stage_bytes;
+  const uint32_t bars = sbase + bar_off;
   auto full = [&](int s) { return bars + 8 * s; };
-  auto afull = [&](int s) { return bars + 8 * (STAGES + s); };
-  auto empty = [&](int s) { return bars + 8 * (2 * STAGES + s); };
-  auto acc_full = [&](int b) { return bars + 8 * (3 * STAGES + b); };
-  auto acc_empty = [&](int b) { return bars + 8 * (3 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bars + 8 * (3 * STAGES + 4);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::BAR_OFF + S::BARS * 8);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::BAR_OFF + S::BARS * 8 + 4);
+  auto afull = [&](int s) { return bars + 8 * (MAX_STAGES + s); };
+  auto empty = [&](int s) { return bars + 8 * (2 * MAX_STAGES + s); };
+  auto acc_full = [&](int b) { return bars + 8 * (3 * MAX_STAGES + b); };
+  auto acc_empty = [&](int b) { return bars + 8 * (3 * MAX_STAGES + 2 + b); };
+  const uint32_t drain_bar = bars + 8 * (3 * MAX_STAGES + 4);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + bar_off + S::BARS * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + bar_off + S::BARS * 8 + 4);
   const WaitCtl ctl{abort_flag, &g_gemm_status};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,12 +175,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&tmap_codes);
       const uint32_t tx = (uint32_t)bn * BK * 2 + S::C_BYTES;
       int it = 0;                   // global K-step counter of this CTA
+      Ring ring;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
         const int mb = tile % p.m_blocks, nb = tile / p.m_blocks;
-        for (int kb = 0; kb < ksteps; kb++, it++) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+        for (int kb = 0; kb < ksteps; kb++, it++, ring.next(STAGES)) {
+          const int s = ring.s;
+          const uint32_t ph = ring.ph;
           if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(full(s), tx);
           tma_load_2d(b_buf(s), &tmap_x, kb * BK, mb * bn, full(s));
@@ -178,6 +200,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BM, bn);
       int it = 0, local = 0;
+      Ring ring;
       bool ok = true;
       // Readiness of stage `it` tested while the previous stage's MMAs were
       // being issued, so the ~180-cycle latency of the test is hidden; only a
@@ -189,9 +212,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!wait_bounded(acc_empty(buf), use ^ 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN_MAX;
-        for (int kb = 0; kb < ksteps; kb++, it++) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
+        for (int kb = 0; kb < ksteps; kb++, it++, ring.next(STAGES)) {
+          const int s = ring.s;
+          const uint32_t ph = ring.ph;
           if (!ready) {
             const bool f = mbar_test(full(s), ph), a = mbar_test(afull(s), ph);
             if (!(f || wait_bounded(full(s), ph, ctl)) || !(a || wait_bounded(afull(s), ph, ctl))) {
@@ -211,8 +234,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // Test the next stage only now: a test (acquire) holds back this
           // thread's later operations until it returns (~250 cycles), which
           // then overlaps the MMAs just issued instead of delaying them.
-          const int sn = (it + 1) % STAGES;
-          const uint32_t phn = ((it + 1) / STAGES) & 1;
+          Ring nx = ring;
+          nx.next(STAGES);
+          const int sn = nx.s;
+          const uint32_t phn = nx.ph;
           const bool fn = mbar_test(full(sn), phn), an = mbar_test(afull(sn), phn);
           ready = fn && an;
         }
@@ -229,9 +254,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int t = threadIdx.x - DQ_WARP0 * 32;      // 0 .. DQ_THREADS - 1
     const int r = t >> 1, part = t & 1;             // weight row within the tile, k half
     const int G = p.groups_per_row;
-    int it = 0;
+    Ring ring;
     bool ok = true;
-    bool ready = false;       // stage `it` seen complete by a test issued one K-step early
+    bool ready = false;       // the current stage seen complete by a test issued one K-step early
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
       const int nb = tile / p.m_blocks;
       const int row = nb * BM + r;
@@ -249,9 +274,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (BITS == 4) bc_nxt = ld_stream_u4(brow + 8);
         }
       }
-      for (int kb = 0; kb < ksteps; kb++, it++) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
+      for (int kb = 0; kb < ksteps; kb++, ring.next(STAGES)) {
+        const int s = ring.s;
+        const uint32_t ph = ring.ph;
         const int g = (kb * BK) >> p.gshift;
         uint16_t sb = 0, bb = 0;
         if (row_ok) {
@@ -300,7 +325,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         // the next stage's readiness, tested early: its result is read after
         // this stage's stores (measured faster than testing after them)
-        const bool next_ready = mbar_test(full((it + 1) % STAGES), ((it + 1) / STAGES) & 1);
+        Ring nx = ring;
+        nx.next(STAGES);
+        const bool next_ready = mbar_test(full(nx.s), nx.ph);
         const uint32_t arow = a_buf(s) + r * 128;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
@@ -455,11 +482,15 @@ cudaError_t launch_bits(const uint16_t *x_bf16, const uint32_t *codes, const Gem
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  GemmParams pp = p;
+  pp.stages = S::stages(p.bn);
+  if (pp.stages < 2) return cudaErrorNotSupported;
+  const int alloc = S::alloc(p.bn);
   auto kern = qmm_gemm_kernel<BITS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alloc);
   if (e != cudaSuccess) return e;
   const int grid = p.tiles < sm_count_gemm() ? p.tiles : sm_count_gemm();
-  kern<<<grid, NUM_THREADS, S::ALLOC, s>>>(tx, tc, p);
+  kern<<<grid, NUM_THREADS, alloc, s>>>(tx, tc, pp);
   return cudaGetLastError();
 }
 
