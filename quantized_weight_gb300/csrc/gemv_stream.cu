@@ -306,16 +306,27 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
     }
   }
   pdl_wait();                                                    // x is written by the previous kernel
-  {
-    // x, once per CTA, coalesced; stored as each lane's register pairs
+  f2 xp[L::PAIRS];
+  if constexpr (BITS == 8) {
+    // INT8: this lane's 16 activations (64 contiguous bytes), loaded
+    // straight into its register pairs (measured faster than staging)
+    const float *src = p.x + seg * L::SEG_W + lane * L::W;
+#pragma unroll
+    for (int i = 0; i < L::W / 4; i++) {
+      const float4 v = ld_nc_f4(src + 4 * i);
+      xp[2 * i] = f2_make(v.x, v.y);
+      xp[2 * i + 1] = f2_make(v.z, v.w);
+    }
+  } else {
+    // INT4: x once per CTA, coalesced, staged in shared memory as each lane's
+    // register pairs (a lane's 128 contiguous bytes load slowly from L1)
     if (p.two_per_sm) stage_x<BITS, 4>(p.x, p.K, xs, ct, nthreads);
     else stage_x<BITS, 1>(p.x, p.K, xs, ct, nthreads);
     // consumer warps only; every consumer thread reaches it (no exit before)
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-  }
-  f2 xp[L::PAIRS];
 #pragma unroll
-  for (int i = 0; i < L::PAIRS; i++) xp[i] = xs[(seg * L::PAIRS + i) * 32 + lane];
+    for (int i = 0; i < L::PAIRS; i++) xp[i] = xs[(seg * L::PAIRS + i) * 32 + lane];
+  }
   float xsum = 0.0f;
   if constexpr (BITS == 4) {
 #pragma unroll
@@ -436,7 +447,7 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   if (grid > sm_count_stream()) grid = sm_count_stream();
   p.rows_per_cta = (int)((N + grid - 1) / grid);            // the largest slab of the even split
   const int coef = p.rows_per_cta * G * 2 * (BITS == 4 ? 2 : 1);
-  const int xbytes = (int)K * 4;
+  const int xbytes = BITS == 8 ? 0 : (int)K * 4;               // INT8 loads x into registers
   const int redb = p.rows_per_cta * p.segs * 4;
   const int fixed = coef + xbytes + redb + 8 * 64;
   int stage_rows0 = STAGE_ROWS_MAX;
