@@ -295,7 +295,7 @@ def measure_extra(name, torch, qmm, stream, pk, reps=20):
     chain = Chain(calls, torch).capture(stream)
     sec = time_graph(chain, reps, 3, torch, stream) / copies
     gbs = nbytes / sec / 1e9
-    del chain, e2e_chain
+    del chain
     torch.cuda.empty_cache()
     return {"kind": kind, "M": M, "N": N, "K": K, "us_per_launch": sec * 1e6, "bytes_per_launch": nbytes,
             "gbs": gbs, "frac_of_measured_hbm": gbs / pk["hbm_gbs"], "copies": copies}
