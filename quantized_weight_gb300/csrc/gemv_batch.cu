@@ -5,9 +5,10 @@
 // page, "Pushing the limits of legacy hardware", section "Use short context to
 // change the state cost", batches decode so the weights are shared).  Each
 // code is therefore unpacked once and used M times, and each activation
-// loaded from shared memory is used for several rows: a lane owns R = 4 rows
-// (32-row block: lane = 8 row slots x 4 k lanes) and, per step, one 32-bit
-// code word of each of its rows and the matching activations of MT tokens.
+// loaded is used for several rows: a lane owns R rows (8R-row block: lane =
+// 8 row slots x 4 k lanes; R = 4, or 2 for the single-pass INT8 path) and,
+// per step, one 32-bit code word of each of its rows and the matching
+// activations of MT tokens.
 // Per step a lane issues 4 code loads and MT (INT8) or 2*MT (INT4) 16-byte
 // activation loads for 4 * MT * (32/bits) multiply-adds.
 //
@@ -16,7 +17,10 @@
 // stride of row_bytes + 16, so the 8 row slots x 4 k lanes of one code load
 // hit 32 distinct banks) into shared memory, before the
 // programmatic-dependent-launch wait.  The activations of MT tokens are
-// staged in shared memory per pass (M > MT takes two passes).  Consumer warps
+// staged in shared memory per pass (M > MT takes two passes), except for
+// INT8 with 5 to 8 tokens: eight tokens of x do not fit beside the slab, so
+// that path reads them from global memory (L1-cached) at each step and takes
+// all tokens in one pass.  Consumer warps
 // take (32-row block, K part) work items; a lane's 4 k lanes are reduced with
 // two shuffles, the K parts of a row in part order: no atomics, the same bits
 // on every run.
@@ -45,8 +49,6 @@ namespace {
 using namespace sm100;
 
 constexpr uint32_t kMagic = 0x4B000000u;   // bit pattern of 2^23
-constexpr int R = 4;                       // rows per lane
-constexpr int kRowsPerBlock = 8 * R;       // 32
 constexpr int kMaxConsumerWarps = 15;   // 16 warps: 4 per scheduler, up to 128 registers each
 constexpr int kThreads = 32 * (kMaxConsumerWarps + 1);
 constexpr int kSmemBudget = 220 * 1024;
@@ -65,9 +67,14 @@ struct BatchParams {
   int off_x, off_coef, off_red, off_bar;
 };
 
-template <int BITS, int MT>
+// R rows per lane (row block of 8 * R rows); MT tokens per pass; XG: the
+// activations are read from global memory (L1-cached) at each step instead
+// of being staged in shared memory (INT8, all tokens in one pass).
+template <int BITS, int MT, int R, bool XG>
 __global__ void __launch_bounds__(kThreads, 1) gemv_batch_kernel(const BatchParams p) {
+  static_assert(!XG || BITS == 8, "global activations only for INT8");
   constexpr int KW = 32 / BITS;                 // weights per code word
+  constexpr int kRowsPerBlock = 8 * R;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_addr(smem);
   float *xs = reinterpret_cast<float *>(smem + p.off_x);                       // [MT][K]
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_batch_kernel(const BatchPara
   bool waited = false;
   for (int m0 = 0; m0 < p.M; m0 += MT) {
     // 1. activations of tokens m0 .. m0+MT-1 (zeros past M), coalesced
-    {
+    if constexpr (!XG) {
       const int units = MT * (p.K / 4);
       for (int u = ct; u < units; u += nthreads) {
         const int m = u / (p.K / 4), k4 = u - m * (p.K / 4);
@@ -190,7 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_batch_kernel(const BatchPara
             f2 x01[MT], x23[MT];
 #pragma unroll
             for (int m = 0; m < MT; m++) {
-              const float4 v = *reinterpret_cast<const float4 *>(xs + m * p.K + 4 * wi);
+              float4 v;
+              if constexpr (XG)   // tokens past M repeat the last one (their sums are not stored)
+                v = ld_nc_f4(p.x + (int64_t)min(m0 + m, p.M - 1) * p.K + 4 * wi);
+              else
+                v = *reinterpret_cast<const float4 *>(xs + m * p.K + 4 * wi);
               x01[m] = f2_make(v.x, v.y);
               x23[m] = f2_make(v.z, v.w);
             }
@@ -278,9 +289,9 @@ int sm_count_batch() {
   return n;
 }
 
-template <int BITS, int MT>
+template <int BITS, int MT, int R, bool XG>
 cudaError_t launch_mt(const BatchParams &p, int grid, int threads, size_t smem, cudaStream_t s) {
-  auto kern = gemv_batch_kernel<BITS, MT>;
+  auto kern = gemv_batch_kernel<BITS, MT, R, XG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -296,12 +307,13 @@ cudaError_t launch_mt(const BatchParams &p, int grid, int threads, size_t smem, 
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-// Shared-memory layout for MT tokens per pass; 0 if it does not fit.
-size_t layout(BatchParams &p, int MT, int bits) {
-  const int rows_max = p.row_blocks * kRowsPerBlock;
+// Shared-memory layout for MT tokens per pass and row blocks of rb rows
+// (activations staged unless xg); 0 if it does not fit.
+size_t layout(BatchParams &p, int MT, int bits, int rb, bool xg) {
+  const int rows_max = p.row_blocks * rb;
   const int code_bytes = rows_max * p.row_stride;
   p.off_x = (code_bytes + 127) & ~127;
-  p.off_coef = p.off_x + MT * p.K * 4;
+  p.off_coef = p.off_x + (xg ? 0 : MT * p.K * 4);
   const int coef_bytes = rows_max * p.G * 2 * (bits == 4 ? 2 : 1);
   p.off_red = (p.off_coef + coef_bytes + 15) & ~15;
   const int red_bytes = rows_max * MT * p.parts * 4;
@@ -337,19 +349,33 @@ cudaError_t launch_gemv_batch(const float *x, const uint32_t *codes, const uint1
   int grid = sm_count_batch();
   if (N < grid) grid = (int)N;
   const int rows_max = (int)((N + grid - 1) / grid);
-  p.row_blocks = (rows_max + kRowsPerBlock - 1) / kRowsPerBlock;
-  if (p.row_blocks > kMaxRowBlocks) return cudaErrorNotSupported;
-  int parts = kMaxConsumerWarps / p.row_blocks;
-  if (parts > p.quads) parts = p.quads;
-  p.parts = parts < 1 ? 1 : parts;
-  const int threads = 32 * (1 + p.row_blocks * p.parts);
+  // row blocks of rb rows; the K parts share the consumer warps
+  auto setup = [&](int rb) {
+    p.row_blocks = (rows_max + rb - 1) / rb;
+    if (p.row_blocks > kMaxRowBlocks) return false;
+    int parts = kMaxConsumerWarps / p.row_blocks;
+    if (parts > p.quads) parts = p.quads;
+    p.parts = parts < 1 ? 1 : parts;
+    return true;
+  };
+  auto threads = [&]() { return 32 * (1 + p.row_blocks * p.parts); };
+  if (bits == 8 && M > 4 && setup(16)) {
+    // INT8, 5..8 tokens: one pass over all of them, 2 rows per lane, the
+    // activations read at each step (8 tokens of x do not fit beside the slab)
+    const size_t smem = layout(p, 8, bits, 16, true);
+    if (smem != 0) return launch_mt<8, 8, 2, true>(p, grid, threads(), smem, s);
+  }
+  if (!setup(32)) return cudaErrorNotSupported;
   // tokens per pass: all M (rounded up to 2 or 4) when they fit, else 4 or 2
   const int want = M <= 2 ? 2 : 4;
   for (int mt = want; mt >= 2; mt /= 2) {
-    const size_t smem = layout(p, mt, bits);
+    const size_t smem = layout(p, mt, bits, 32, false);
     if (smem == 0) continue;
-    if (bits == 8) return mt == 4 ? launch_mt<8, 4>(p, grid, threads, smem, s) : launch_mt<8, 2>(p, grid, threads, smem, s);
-    return mt == 4 ? launch_mt<4, 4>(p, grid, threads, smem, s) : launch_mt<4, 2>(p, grid, threads, smem, s);
+    if (bits == 8)
+      return mt == 4 ? launch_mt<8, 4, 4, false>(p, grid, threads(), smem, s)
+                     : launch_mt<8, 2, 4, false>(p, grid, threads(), smem, s);
+    return mt == 4 ? launch_mt<4, 4, 4, false>(p, grid, threads(), smem, s)
+                   : launch_mt<4, 2, 4, false>(p, grid, threads(), smem, s);
   }
   return cudaErrorNotSupported;
 }

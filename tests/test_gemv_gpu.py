@@ -156,7 +156,9 @@ def test_chained_products_see_the_previous_output(qmm):
 # small-batch decode at MLP-projection shapes: several 32-row blocks per SM,
 # one or two token passes, ragged row blocks
 BATCH = [(2, 6144, 2048, 4, 64), (4, 6144, 2048, 4, 64), (8, 2048, 6144, 4, 64), (3, 8192, 4096, 8, 64),
-         (8, 8192, 1024, 8, 32), (5, 4100, 2048, 8, 128), (7, 1000, 4096, 4, 128)]
+         (8, 8192, 1024, 8, 32), (5, 4100, 2048, 8, 128), (7, 1000, 4096, 4, 128),
+         # INT8, 5..8 tokens in one pass: the benchmark shape, fewer rows than SMs, a ragged slab
+         (8, 4096, 4096, 8, 64), (6, 150, 512, 8, 64), (7, 2333, 3072, 8, 64)]
 
 
 @pytest.mark.parametrize("M,N,K,bits,group", BATCH)
