@@ -168,21 +168,21 @@ __global__ void __launch_bounds__(kThreads) gather_dequant_kernel(
 
 // ---------------------------------------------------------------- quantizer
 
-// Total order on non-NaN floats for the group's range: -0 below +0, so the
-// stored bias does not depend on the order of the reduction.
-__device__ __forceinline__ float qmin(float a, float b) {
-  if (isnan(a)) return b;
-  if (isnan(b)) return a;
-  if (a < b) return a;
-  if (b < a) return b;
-  return signbit(a) ? a : b;
+// The group's range takes NaN-free values in a total order with -0 below
+// +0, so the stored bias does not depend on the order of the reduction.  The
+// order is that of these integer keys (the sign-magnitude bits with the
+// magnitude flipped for negative values), compared with one integer min/max.
+__device__ __forceinline__ int order_key(float f) {
+  const int b = __float_as_int(f);
+  return b ^ ((b >> 31) & 0x7FFFFFFF);
 }
-__device__ __forceinline__ float qmax(float a, float b) {
-  if (isnan(a)) return b;
-  if (isnan(b)) return a;
-  if (a > b) return a;
-  if (b > a) return b;
-  return signbit(a) ? b : a;
+__device__ __forceinline__ float from_order_key(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
+
+// Approximate reciprocal (relative error within a few units in the last place).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 // binary16 bits of f, round to nearest even; any NaN becomes 0x7E00.
@@ -220,26 +220,48 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float *__restr
 #pragma unroll
       for (int j = 0; j < 8; j++) v[j] = __int_as_float(0x7FC00000);
     }
-    float lo = v[0], hi = v[0];
+    int kmin = 0x7FFFFFFF, kmax = (int)0x80000000;            // no value yet (NaN weights are skipped)
 #pragma unroll
-    for (int j = 1; j < 8; j++) lo = qmin(lo, v[j]), hi = qmax(hi, v[j]);
+    for (int j = 0; j < 8; j++)
+      if (!isnan(v[j])) {
+        const int k = order_key(v[j]);
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+      }
 #pragma unroll
     for (int o = 1; o < GT; o <<= 1) {
-      lo = qmin(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = qmax(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     }
     if (!active) continue;
+    const float nan = __int_as_float(0x7FC00000);
+    const float lo = kmin == 0x7FFFFFFF ? nan : from_order_key(kmin);   // an all-NaN group has a NaN range
+    const float hi = kmax == (int)0x80000000 ? nan : from_order_key(kmax);
     const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
     const uint16_t sh = half_bits_rn(s32), bh = half_bits_rn(lo);
     const float s = h2f(sh), b = h2f(bh);
     uint32_t word = 0;
     if (s > 0.0f && isfinite(s)) {
+      // The quotient (w - b) / s, correctly rounded, decides q only through
+      // roundf, i.e. only where it lies next to a half-integer.  A product
+      // with the approximate reciprocal is within a few units in the last
+      // place of it; where that product is farther than 1e-5 (relative) from
+      // the nearest half-integer both round alike, elsewhere the correctly
+      // rounded division is taken.
+      // A NaN weight gives a NaN quotient, which clamps to 0; an infinite one
+      // takes the division and clamps to 0 or 15.
+      const float inv = rcp_approx(s);
 #pragma unroll
       for (int j = 0; j < 8; j++) {
-        if (isnan(v[j])) continue;
-        float r = roundf(__fdiv_rn(__fsub_rn(v[j], b), s));
+        const float d = __fsub_rn(v[j], b);
+        const float qf = __fmul_rn(d, inv);
+        const float fl = floorf(qf);
+        const float fr = qf - fl;                 // exact, except just below 0 where only the check needs it
+        float r;
+        if (fabsf(fr - 0.5f) > 1e-5f * fmaxf(1.0f, fabsf(qf))) r = fr > 0.5f ? fl + 1.0f : fl;   // = roundf(qf)
+        else r = roundf(__fdiv_rn(d, s));
         r = fminf(fmaxf(r, 0.0f), 15.0f);
-        word |= (uint32_t)r << (4 * j);
+        word |= (__float_as_uint(r + 8388608.0f) & 0xFu) << (4 * j);   // the integer r in the low mantissa bits
       }
     }
     packed[i] = word;

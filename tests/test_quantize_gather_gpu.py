@@ -67,6 +67,38 @@ def test_quantize_edge_groups(qmm, oracle_mod):
     assert rb[3, 0] == 0x7E00 and (c[3, :64] == 0).all()
 
 
+def test_quantize_quotients_next_to_half_integers(qmm, oracle_mod):
+    """Weights placed a few float32 steps from b + (k + 1/2) * s, with scales
+    that are not powers of two: the quotient (w - b) / s then sits next to a
+    rounding boundary, where only the correctly rounded division decides q."""
+    rng = np.random.default_rng(23)
+    rows = []
+    while len(rows) < 96:
+        b16 = np.float16(rng.uniform(-1.0, 0.0))
+        s16 = np.float16(rng.uniform(0.003, 0.05))
+        b, sc = np.float32(b16), np.float32(s16)
+        mx = np.float32(np.float64(b) + 15.0 * np.float64(sc))
+        if np.float16(np.float32(np.float32(mx - b) / np.float32(15.0))) != s16:
+            continue                                   # the group's own range must give back this scale
+        row = np.empty(64, np.float32)
+        row[0], row[1] = b, mx
+        for i in range(2, 64):
+            k = i % 15
+            if i % 4 == 0:                              # just outside +-1e-5 of the half-integer
+                off = (2e-5 if i % 8 == 0 else -2e-5) * max(1.0, k + 0.5)
+                row[i] = np.float32(np.float64(b) + (k + 0.5 + off) * np.float64(sc))
+                continue
+            t = np.float32(np.float64(b) + (k + 0.5) * np.float64(sc))
+            for _ in range(int(rng.integers(0, 4))):    # up to three steps up or down
+                t = np.nextafter(t, np.float32(np.inf) if i % 2 else np.float32(-np.inf), dtype=np.float32)
+            row[i] = t
+        rows.append(row)
+    w = np.stack(rows)
+    c, s, b, rc, rs, rb = _quantize_both(qmm, oracle_mod, w, 64)
+    assert np.array_equal(s, rs) and np.array_equal(b, rb)
+    assert np.array_equal(c, rc)
+
+
 def test_quantize_then_products_roundtrip(qmm, oracle_mod):
     """Quantized weights feed the products unchanged: the GPU product of the
     GPU-quantized matrix equals the oracle product of the oracle-quantized one."""
