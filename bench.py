@@ -407,9 +407,19 @@ def profile_workload(name, launches):
     from quantized_weight_gb300 import build as qbuild
     from quantized_weight_gb300 import qmm
     qbuild.build()
-    w, d, t = device_inputs(name, 0, torch, qmm)
-    y = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
-    f = (gemm_call if w.prefill else gemv_call)(qmm, t, w, y)
+    if name in EXTRA_WORKLOADS and EXTRA_WORKLOADS[name][0] == "argmax":
+        _, M, N, K = EXTRA_WORKLOADS[name]
+        d = inputs.make(M, N, K, 4, 64, 0)
+        t = {"x": torch.from_numpy(d["x"]).cuda(),
+             "packed": qmm.pack(torch.from_numpy(d["codes"]).cuda(), 4),
+             "scales": torch.from_numpy(d["scales"].view(np.float16)).cuda(),
+             "biases": torch.from_numpy(d["biases"].view(np.float16)).cuda()}
+        ws = qmm.argmax_workspace(M, N)
+        f = lambda: qmm.gemv_argmax(t["x"], t["packed"], t["scales"], t["biases"], N, 4, 64, ws)
+    else:
+        w, d, t = device_inputs(name, 0, torch, qmm)
+        y = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+        f = (gemm_call if w.prefill else gemv_call)(qmm, t, w, y)
     for _ in range(launches):
         f()
     qmm.check()

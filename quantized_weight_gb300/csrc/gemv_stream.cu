@@ -53,7 +53,10 @@ constexpr int RG = 4;                      // rows per group (one butterfly)
 constexpr int STAGE_ROWS_MAX = 16;         // rows per code stage
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kSmemPair = 108 * 1024;      // leaves room for two CTAs per SM
+constexpr int kAmScratch = 8 * 32;         // argmax scratch: two words per consumer warp
 constexpr int kMaxConsumerWarps = 15;
+constexpr int kMaxConsumerWarpsWide = 31;  // long slabs: one CTA per SM, 32 warps
+constexpr int kWideRows = 128;             // slabs longer than this take the wide layout
 
 template <int BITS>
 struct Lane {
@@ -78,6 +81,8 @@ struct StreamParams {
   int stages;          // ring depth
   int rows_per_cta;
   int two_per_sm;      // two CTAs fit on an SM (so the next product's copies start early)
+  int wide;            // long slab: wide layout (see the kernel)
+  int stage_bytes;     // bytes per ring stage (codes, then in the wide layout the stage's coefficients)
   // shared-memory layout (bytes from the 128-byte-aligned base)
   int off_coef, off_x, off_red, off_bar, off_am;
   ArgmaxWork am;       // used by the argmax epilogue only
@@ -208,13 +213,19 @@ __device__ __forceinline__ void stage_x(const float *__restrict__ x, int K, f2 *
   }
 }
 
-template <int BITS, bool ARGMAX>
-__global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams p) {
+// WIDE (slabs longer than kWideRows rows, e.g. a vocabulary head): up to 31
+// consumer warps, a deep ring, and the coefficients of each stage's rows
+// copied with its codes (a whole slab's coefficients would crowd out the
+// ring).  Otherwise: up to 15 consumer warps, two CTAs per SM where they fit,
+// the slab's coefficients copied once.
+template <int BITS, bool ARGMAX, bool WIDE>
+__global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_kernel(const StreamParams p) {
   using L = Lane<BITS>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.stages;
   const uint32_t sbase = smem_addr(smem);
   const int code_stage_bytes = p.stage_rows * p.row_bytes;
+  const int cbytes_row = p.G * 2;                                 // one coefficient row (scales or biases)
   const uint16_t *sc = reinterpret_cast<const uint16_t *>(smem + p.off_coef);
   const uint16_t *bi = sc + p.rows_per_cta * p.G;
   f2 *xs = reinterpret_cast<f2 *>(smem + p.off_x);                 // [segs][PAIRS][32 lanes]
@@ -252,12 +263,16 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const uint32_t gbytes = (uint32_t)rows * p.G * 2;
-      mbar_arrive_expect_tx(coef_full, gbytes * (BITS == 4 ? 2 : 1));
-      bulk_load(sbase + p.off_coef, p.scales + (int64_t)n_begin * p.G, gbytes, coef_full, pol);
-      if (BITS == 4)
-        bulk_load(sbase + p.off_coef + p.rows_per_cta * p.G * 2, p.biases + (int64_t)n_begin * p.G, gbytes,
-                  coef_full, pol);
+      if constexpr (!WIDE) {
+        const uint32_t gbytes = (uint32_t)rows * p.G * 2;
+        mbar_arrive_expect_tx(coef_full, gbytes * (BITS == 4 ? 2 : 1));
+        bulk_load(sbase + p.off_coef, p.scales + (int64_t)n_begin * p.G, gbytes, coef_full, pol);
+        if (BITS == 4)
+          bulk_load(sbase + p.off_coef + p.rows_per_cta * p.G * 2, p.biases + (int64_t)n_begin * p.G, gbytes,
+                    coef_full, pol);
+      } else {
+        mbar_arrive(coef_full);                                  // the coefficients come with the stages
+      }
       int j = 0;
       bool ok = true;
       for (; j < nst; j++) {
@@ -265,10 +280,19 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
         const uint32_t ph = (j / S) & 1;
         if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
         const int r0 = j * p.stage_rows;
-        const uint32_t cbytes = (uint32_t)min(p.stage_rows, rows - r0) * p.row_bytes;
-        mbar_arrive_expect_tx(full(s), cbytes);
-        bulk_load(sbase + s * code_stage_bytes, p.codes + (int64_t)(n_begin + r0) * p.row_bytes, cbytes, full(s),
-                  pol);
+        const int nr = min(p.stage_rows, rows - r0);
+        const uint32_t cbytes = (uint32_t)nr * p.row_bytes;
+        const uint32_t gbytes = (uint32_t)(nr * cbytes_row);
+        const uint32_t dst = sbase + s * p.stage_bytes;
+        mbar_arrive_expect_tx(full(s), cbytes + (WIDE ? gbytes * (BITS == 4 ? 2 : 1) : 0));
+        bulk_load(dst, p.codes + (int64_t)(n_begin + r0) * p.row_bytes, cbytes, full(s), pol);
+        if constexpr (WIDE) {
+          // the stage's scale (and bias) rows, after its codes
+          bulk_load(dst + code_stage_bytes, p.scales + (int64_t)(n_begin + r0) * p.G, gbytes, full(s), pol);
+          if (BITS == 4)
+            bulk_load(dst + code_stage_bytes + p.stage_rows * cbytes_row, p.biases + (int64_t)(n_begin + r0) * p.G,
+                      gbytes, full(s), pol);
+        }
       }
       if (!ok) {
         const int first = j > S ? j - S : 0;
@@ -340,14 +364,39 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
   const int lane_off = seg * L::SEG_BYTES + lane * L::BYTES;
   if (!p.two_per_sm) ok = __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
 
+  // the group's stage j, ring slot s and phase ph (where a warp walks many
+  // groups, a wide slab or INT8 with one warp per segment, they advance
+  // without a division; measured slower for the short INT4 slabs)
+  int j = t0 / groups_per_stage, jrem = t0 - j * groups_per_stage;
+  int s = j % S;
+  uint32_t ph = (j / S) & 1;
   for (int grp = t0; ok && grp < ngroups; grp += p.wps) {
-    const int j = grp / groups_per_stage;                        // stage holding this group
-    const int s = j % S;
-    const uint32_t ph = (j / S) & 1;
+    if constexpr (WIDE || BITS != 4) {
+      if (grp != t0) {
+        jrem += p.wps;
+        while (jrem >= groups_per_stage) {
+          jrem -= groups_per_stage;
+          j++;
+          if (++s == S) s = 0, ph ^= 1u;
+        }
+      }
+    } else {
+      j = grp / groups_per_stage;
+      s = j % S;
+      ph = (j / S) & 1;
+    }
     if (j > prewaited && !__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
     const int rbase = grp * RG;                                  // first row (within the CTA)
     const int nr = min(RG, rows - rbase);
-    const uint8_t *st = smem + s * code_stage_bytes + (rbase - j * p.stage_rows) * p.row_bytes;
+    const uint8_t *st = smem + s * p.stage_bytes + (rbase - j * p.stage_rows) * p.row_bytes;
+    // this group's coefficient rows: in the stage (wide layout), or in the slab
+    const uint16_t *scg = sc, *big = bi;
+    int crow = rbase;
+    if constexpr (WIDE) {
+      scg = reinterpret_cast<const uint16_t *>(smem + s * p.stage_bytes + code_stage_bytes);
+      big = scg + p.stage_rows * p.G;
+      crow = rbase - j * p.stage_rows;
+    }
     float part[RG];
     if constexpr (BITS == 4) {
 #pragma unroll
@@ -356,16 +405,16 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const StreamParams 
         float da, db;
         dot2_int4(*reinterpret_cast<const uint4 *>(st + ra * p.row_bytes + lane_off),
                   *reinterpret_cast<const uint4 *>(st + rb * p.row_bytes + lane_off), xp, da, db);
-        const int ia = (rbase + ra) * p.G + g, ib = (rbase + rb) * p.G + g;
-        part[rr] = fmaf(h2f(sc[ia]), da, h2f(bi[ia]) * xsum);
-        part[rr + 1] = fmaf(h2f(sc[ib]), db, h2f(bi[ib]) * xsum);
+        const int ia = (crow + ra) * p.G + g, ib = (crow + rb) * p.G + g;
+        part[rr] = fmaf(h2f(scg[ia]), da, h2f(big[ia]) * xsum);
+        part[rr + 1] = fmaf(h2f(scg[ib]), db, h2f(big[ib]) * xsum);
       }
     } else {
 #pragma unroll
       for (int rr = 0; rr < RG; rr++) {
         const int r = rr < nr ? rr : 0;
         const uint8_t *cp = st + r * p.row_bytes + lane_off;
-        const float sv = h2f(sc[(rbase + r) * p.G + g]);
+        const float sv = h2f(scg[(crow + r) * p.G + g]);
         if constexpr (BITS == 8) {
           part[rr] = sv * dot_int8(*reinterpret_cast<const uint4 *>(cp), xp);
         } else {
@@ -442,43 +491,49 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   p.gshift = __builtin_ctz((unsigned)group);
   p.row_bytes = (int)(K * BITS / 8);
   p.segs = (int)(K / L::SEG_W);
-  if (p.segs > kMaxConsumerWarps) return false;
   grid = (int)((N + RG - 1) / RG);
   if (grid > sm_count_stream()) grid = sm_count_stream();
   p.rows_per_cta = (int)((N + grid - 1) / grid);            // the largest slab of the even split
-  const int coef = p.rows_per_cta * G * 2 * (BITS == 4 ? 2 : 1);
+  p.wide = p.rows_per_cta > kWideRows ? 1 : 0;
+  const int max_warps = p.wide ? kMaxConsumerWarpsWide : kMaxConsumerWarps;
+  if (p.segs > max_warps) return false;
+  const int coef_row = G * 2 * (BITS == 4 ? 2 : 1);              // coefficient bytes per row
+  const int coef = p.wide ? 0 : p.rows_per_cta * coef_row;      // the slab's, copied once
+  const int srow = p.row_bytes + (p.wide ? coef_row : 0);        // ring bytes per row
   const int xbytes = BITS == 8 ? 0 : (int)K * 4;               // INT8 loads x into registers
   const int redb = p.rows_per_cta * p.segs * 4;
-  const int fixed = coef + xbytes + redb + 8 * 64;
+  const int fixed = coef + xbytes + redb + 8 * 64 + kAmScratch;
   int stage_rows0 = STAGE_ROWS_MAX;
   while (stage_rows0 > RG && stage_rows0 / 2 >= p.rows_per_cta) stage_rows0 /= 2;
   // Prefer a ring small enough for two CTAs per SM (the next product's CTA
   // then starts, and its first copies land, while this one still runs), as
   // long as it keeps two stages in flight; else the deepest ring that fits.
+  // A wide slab takes the deepest ring that fits.
   int S = 0;
-  for (int sr = stage_rows0; sr >= RG && S == 0; sr /= 2) {
+  for (int sr = stage_rows0; !p.wide && sr >= RG && S == 0; sr /= 2) {
     const int nst = (p.rows_per_cta + sr - 1) / sr;
-    int s2 = (kSmemPair - fixed) / (sr * p.row_bytes);
+    int s2 = (kSmemPair - fixed) / (sr * srow);
     if (s2 > nst) s2 = nst;
     if (s2 >= 2 || s2 == nst) S = s2, p.stage_rows = sr;
   }
   if (S < 1) {
     p.stage_rows = stage_rows0;
     const int nst = (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows;
-    S = (kSmemBudget - fixed) / (p.stage_rows * p.row_bytes);
+    S = (kSmemBudget - fixed) / (p.stage_rows * srow);
     if (S > nst) S = nst;
   }
   if (S < 1) return false;
-  const int stage_bytes = p.stage_rows * p.row_bytes;
+  const int stage_bytes = p.stage_rows * srow;
+  p.stage_bytes = stage_bytes;
   p.stages = S;
   p.off_coef = S * stage_bytes;
   p.off_x = (p.off_coef + coef + 15) & ~15;
   p.off_red = p.off_x + xbytes;
   p.off_bar = (p.off_red + redb + 7) & ~7;
   p.off_am = (p.off_bar + 8 * (2 * S + 2) + 16 + 15) & ~15;
-  smem = (size_t)p.off_am + 8 * 16;
+  smem = (size_t)p.off_am + kAmScratch;
   p.two_per_sm = 2 * (smem + 1024) <= 228 * 1024 ? 1 : 0;   // 1 KB reserved per CTA
-  int wps = kMaxConsumerWarps / p.segs;
+  int wps = max_warps / p.segs;
   const int ngroups = (p.rows_per_cta + RG - 1) / RG;
   if (wps > ngroups) wps = ngroups;
   if (wps < 1) wps = 1;
@@ -487,9 +542,9 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   return true;
 }
 
-template <int BITS, bool ARGMAX>
-cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t smem, cudaStream_t s) {
-  auto kern = gemv_stream_kernel<BITS, ARGMAX>;
+template <int BITS, bool ARGMAX, bool WIDE>
+cudaError_t launch_stream_as(const StreamParams &p0, int grid, int threads, size_t smem, cudaStream_t s) {
+  auto kern = gemv_stream_kernel<BITS, ARGMAX, WIDE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // Every instantiation asks for the same (largest) shared-memory carveout, so
@@ -510,10 +565,16 @@ cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t 
   return cudaLaunchKernelEx(&cfg, kern, p0);
 }
 
+template <int BITS, bool ARGMAX>
+cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t smem, cudaStream_t s) {
+  return p0.wide ? launch_stream_as<BITS, ARGMAX, true>(p0, grid, threads, smem, s)
+                 : launch_stream_as<BITS, ARGMAX, false>(p0, grid, threads, smem, s);
+}
+
 }  // namespace
 
 // Returns cudaErrorNotSupported when the shape does not fit this kernel's
-// layout (K not a whole number of warp segments, more than 15 segments,
+// layout (K not a whole number of warp segments, more segments than consumer warps,
 // coefficient rows not 16-byte multiples, or a slab too large for shared
 // memory); the caller then uses the register-fed kernel.
 cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint16_t *scales,

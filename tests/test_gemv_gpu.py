@@ -161,6 +161,18 @@ BATCH = [(2, 6144, 2048, 4, 64), (4, 6144, 2048, 4, 64), (8, 2048, 6144, 4, 64),
          (8, 4096, 4096, 8, 64), (6, 150, 512, 8, 64), (7, 2333, 3072, 8, 64)]
 
 
+# M = 1 slabs whose coefficients travel with each code stage (more than 16 KB
+# of coefficients per CTA), a ragged last stage included
+STAGED = [(40000, 1024, 4, 64), (40013, 1024, 4, 32), (41000, 4096, 8, 64)]
+
+
+@pytest.mark.parametrize("N,K,bits,group", STAGED)
+def test_large_slabs_with_staged_coefficients(qmm, oracle_mod, N, K, bits, group):
+    y, ref, t, p, d = run_case(qmm, oracle_mod, 1, N, K, bits, group, seed=N + K)
+    assert np.all(np.abs(y - ref) <= fp32_bound(d, bits, group)), (N, K, bits, group)
+    assert rel_l2_rows(y, ref) <= TOL
+
+
 @pytest.mark.parametrize("M,N,K,bits,group", BATCH)
 def test_small_batch_projection_shapes(qmm, oracle_mod, M, N, K, bits, group):
     y, ref, t, p, d = run_case(qmm, oracle_mod, M, N, K, bits, group, seed=M + N + K)
