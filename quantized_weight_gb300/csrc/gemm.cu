@@ -115,7 +115,7 @@ struct GemmParams {
   int m_blocks, n_blocks, tiles;
 };
 
-template <int BITS>
+template <int BITS, bool G64>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     qmm_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     const __grid_constant__ CUtensorMap tmap_codes, const GemmParams p) {
@@ -274,12 +274,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (BITS == 4) bc_nxt = ld_stream_u4(brow + 8);
         }
       }
-      for (int kb = 0; kb < ksteps; kb++, ring.next(STAGES)) {
+      // G64 (group 64 = one K-step, 16-byte coefficient loads): the K-steps
+      // go eight at a time, unrolled, so each step's half of the chunk's
+      // 16-byte coefficient vector is picked out at compile time
+      constexpr int UN = G64 ? 8 : 1;
+      for (int kb0 = 0; kb0 < ksteps && ok; kb0 += UN) {
+#pragma unroll
+      for (int u = 0; u < UN; u++) {
+        const int kb = kb0 + u;
+        if (UN > 1 && kb >= ksteps) break;
         const int s = ring.s;
         const uint32_t ph = ring.ph;
         const int g = (kb * BK) >> p.gshift;
         uint16_t sb = 0, bb = 0;
-        if (row_ok) {
+        if (G64) {
+          if (row_ok) {
+            if (u == 0 && kb0 > 0) {                    // the next chunk of eight groups
+              sc_cur = sc_nxt;
+              bc_cur = bc_nxt;
+              if (kb0 + 8 < G) {
+                sc_nxt = ld_stream_u4(srow + kb0 + 8);
+                if (BITS == 4) bc_nxt = ld_stream_u4(brow + kb0 + 8);
+              }
+            }
+            sb = half_at(sc_cur, u);
+            if (BITS == 4) bb = half_at(bc_cur, u);
+          }
+        } else if (row_ok) {
           if (p.coef_vec) {
             if ((g >> 3) != cur_chunk) {
               cur_chunk = g >> 3;
@@ -344,6 +365,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_proxy_async_smem();
         mbar_arrive(afull(s));
         ready = __all_sync(0xffffffffu, next_ready);
+        ring.next(STAGES);
+      }
       }
     }
   } else {
@@ -486,7 +509,7 @@ cudaError_t launch_bits(const uint16_t *x_bf16, const uint32_t *codes, const Gem
   pp.stages = S::stages(p.bn);
   if (pp.stages < 2) return cudaErrorNotSupported;
   const int alloc = S::alloc(p.bn);
-  auto kern = qmm_gemm_kernel<BITS>;
+  auto kern = (p.gshift == 6 && p.coef_vec) ? qmm_gemm_kernel<BITS, true> : qmm_gemm_kernel<BITS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alloc);
   if (e != cudaSuccess) return e;
   const int grid = p.tiles < sm_count_gemm() ? p.tiles : sm_count_gemm();
