@@ -158,7 +158,9 @@ def test_chained_products_see_the_previous_output(qmm):
 BATCH = [(2, 6144, 2048, 4, 64), (4, 6144, 2048, 4, 64), (8, 2048, 6144, 4, 64), (3, 8192, 4096, 8, 64),
          (8, 8192, 1024, 8, 32), (5, 4100, 2048, 8, 128), (7, 1000, 4096, 4, 128),
          # INT8, 5..8 tokens in one pass: the benchmark shape, fewer rows than SMs, a ragged slab
-         (8, 4096, 4096, 8, 64), (6, 150, 512, 8, 64), (7, 2333, 3072, 8, 64)]
+         (8, 4096, 4096, 8, 64), (6, 150, 512, 8, 64), (7, 2333, 3072, 8, 64),
+         # INT8 at the benchmark's two tokens, ragged slabs of 10-16 rows
+         (2, 4096, 4096, 8, 64), (4, 3000, 2048, 8, 64), (3, 4864, 1024, 8, 32), (6, 2500, 512, 8, 128)]
 
 
 # M = 1 slabs whose coefficients travel with each code stage (more than 16 KB
