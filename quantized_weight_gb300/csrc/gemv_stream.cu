@@ -7,13 +7,17 @@
 // SM) owns a contiguous slab of rows and one producer thread streams the slab
 // into shared memory with a handful of large bulk async copies (the TMA
 // engine; completion counted on mbarriers): the coefficients of all the slab's
-// rows, then the codes in stages of up to 16 rows.  The weights do not depend
-// on the previous kernel in the stream, so the producer runs before the
-// programmatic-dependent-launch wait and a chain of decode products keeps HBM
-// streaming across kernel boundaries.
+// rows, then the codes in stages of up to 16 rows (for slabs over 128 rows,
+// the wide layout: each stage's coefficient rows come with its codes).  The
+// weights do not depend on the previous kernel in the stream, so the producer
+// runs before the programmatic-dependent-launch wait; where two CTAs fit on an
+// SM, a chain of decode products keeps HBM streaming across kernel
+// boundaries, and the consumers also wait for the coefficients and first code
+// stages before that wait.
 //
-// After that wait, the consumer warps load x once per CTA with coalesced
-// loads into a transposed shared-memory layout; each warp then owns one
+// After that wait, the consumer warps load x once per CTA (INT4: coalesced
+// loads into a transposed shared-memory layout; INT8: each lane's 16 values
+// straight into registers); each warp then owns one
 // K-segment (32 lanes x 16 bytes of codes: 1024 INT4, 512 INT8 or, with 4-byte
 // lanes, 1024 Q1 weights) and keeps that segment's activations in registers.
 // A warp takes every wps-th group of 4 rows of the slab; per group the lanes
@@ -240,8 +244,8 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int consumers = p.segs * p.wps;
   // rows split evenly over the grid (one CTA per SM): every SM gets the
-  // same work, and under programmatic dependent launch every SM has room for
-  // exactly one CTA of the next product
+  // same work, and under programmatic dependent launch an SM with room for a
+  // second CTA takes one of the next product
   const int n_begin = (int)((int64_t)blockIdx.x * p.N / gridDim.x);
   const int rows = (int)((int64_t)(blockIdx.x + 1) * p.N / gridDim.x) - n_begin;   // <= rows_per_cta
   const int nst = (rows + p.stage_rows - 1) / p.stage_rows;
