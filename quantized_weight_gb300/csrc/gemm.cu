@@ -29,9 +29,13 @@
 // The MMA computes D[128 weight rows, BN tokens] = A * B^T with A = the
 // dequantized weight tile and B = the x tile, i.e. the transpose of a y tile;
 // putting the weights on the M side lets one dequantized tile serve BN tokens.
-// BN (a multiple of 16, at most 256) is chosen per call so that the tiles
-// fill whole waves of the SMs.  Two accumulators of 256 columns live in TMEM
-// so the epilogue of one tile overlaps the main loop of the next.  Stage
+// BN (a multiple of 16 up to 256, or for INT4 / INT8 of 32 up to 512) is
+// chosen per call (pick_bn).  Up to 256, two accumulators of 256 columns live
+// in TMEM so the epilogue of one tile overlaps the main loop of the next;
+// wider tiles are two MMAs per k-slice (two x boxes of BN/2 rows) into one
+// accumulator of BN columns, which dequantizes each weight tile for more
+// tokens: on the M = 1024 shapes one wave of 3 x 48 tiles instead of two
+// waves of 6 x 48.  Stage
 // buffers are guarded by mbarriers (TMA -> full, dequant -> afull,
 // MMA commit -> empty).
 //
@@ -58,7 +62,8 @@ using namespace sm100;
 
 constexpr int BM = 128;                // weight rows per tile (MMA M)
 constexpr int BK = 64;                 // k per stage: one 128-byte swizzle atom of bf16
-constexpr int BN_MAX = 256;            // tokens per tile (MMA N), at most
+constexpr int BN_MAX = 256;            // tokens per MMA (N), at most
+constexpr int BN_WIDE_MAX = 512;       // tokens per tile, as two MMAs of up to 256 into one accumulator
 constexpr int MAX_STAGES = 8;           // ring depth: as many stages as shared memory holds
 constexpr int SMEM_LIMIT = 227 * 1024;    // dynamic shared memory per CTA
 constexpr int UMMA_K = 16;
@@ -111,11 +116,12 @@ struct GemmParams {
   int groups_per_row;
   int coef_vec;          // coefficient rows load as 16-byte vectors
   int bn;
+  int nsub, bn_sub;      // MMAs per k-slice (1, or 2 for tiles wider than 256) and tokens per MMA
   int stages;            // ring depth
   int m_blocks, n_blocks, tiles;
 };
 
-template <int BITS, bool G64>
+template <int BITS, bool G64, int NSUB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     qmm_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     const __grid_constant__ CUtensorMap tmap_codes, const GemmParams p) {
@@ -184,7 +190,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t ph = ring.ph;
           if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
           mbar_arrive_expect_tx(full(s), tx);
-          tma_load_2d(b_buf(s), &tmap_x, kb * BK, mb * bn, full(s));
+#pragma unroll
+          for (int h = 0; h < NSUB; h++)     // the x tile in boxes of bn_sub rows
+            tma_load_2d(b_buf(s) + h * p.bn_sub * (BK * 2), &tmap_x, kb * BK, mb * bn + h * p.bn_sub, full(s));
           const int cx = BITS == 1 ? (kb >> 1) * S::CB : kb * S::CB;   // byte column of the code chunk
           tma_load_2d(c_buf(s), &tmap_codes, cx, nb * BM, full(s));
         }
@@ -198,7 +206,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, bn);
+      const uint32_t idesc = idesc_bf16_f32(BM, p.bn_sub);
+      constexpr int nbuf = NSUB == 1 ? 2 : 1;   // a tile wider than 256 fills TMEM: one accumulator
       int it = 0, local = 0;
       Ring ring;
       bool ok = true;
@@ -207,8 +216,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // stage found not ready takes the blocking (bounded) wait.
       bool ready = false;
       for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, local++) {
-        const int buf = local & 1;
-        const uint32_t use = (local >> 1) & 1;
+        const int buf = local % nbuf;
+        const uint32_t use = (local / nbuf) & 1;
         if (!wait_bounded(acc_empty(buf), use ^ 1, ctl)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN_MAX;
@@ -226,9 +235,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint64_t ad = smem_desc_sw128(a_buf(s));
           const uint64_t bd = smem_desc_sw128(b_buf(s));
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; kk++) {
-            // +32 bytes per 16 k inside the swizzle atom: +2 in the encoded address
-            umma_bf16(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          for (int h = 0; h < NSUB; h++) {
+            // sub-tile h: tokens h*bn_sub.., rows of 128 bytes (address field in 16-byte units)
+            const uint64_t bdh = bd + (uint64_t)(h * p.bn_sub * (BK * 2 / 16));
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; kk++) {
+              // +32 bytes per 16 k inside the swizzle atom: +2 in the encoded address
+              umma_bf16(d_tmem + h * p.bn_sub, ad + 2 * kk, bdh + 2 * kk, idesc, (kb | kk) != 0);
+            }
           }
           umma_commit(empty(s));          // stage free once these MMAs have read it
           // Test the next stage only now: a test (acquire) holds back this
@@ -375,10 +389,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = q * 32 + lane;                     // weight row within the tile
     int local = 0;
     bool ok = true;
+    constexpr int nbuf = NSUB == 1 ? 2 : 1;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, local++) {
       const int mb = tile % p.m_blocks, nb = tile / p.m_blocks;
-      const int buf = local & 1;
-      const uint32_t use = (local >> 1) & 1;
+      const int buf = local % nbuf;
+      const uint32_t use = (local / nbuf) & 1;
       if (!__all_sync(0xffffffffu, wait_bounded(acc_full(buf), use, ctl))) { ok = false; break; }
       tc_fence_after();
       const int n = nb * BM + r;
@@ -451,19 +466,25 @@ int sm_count_gemm() {
   return n;
 }
 
-// Token-tile width: the multiple of 16 (<= 256) that minimizes
-// waves * max(BN, floor), where a wave is one tile per SM and `floor` stands
-// for the per-K-step dequantization time below which a narrower tile does not
-// get faster.  Ties go to the wider tile.
-int pick_bn(int64_t M, int64_t N, int sms) {
+// Token-tile width: a multiple of 16 up to 256, or of 32 up to 512 (two MMAs
+// per k-slice, where allowed and a ring of three stages still fits), that
+// minimizes waves * (C0 + BN): a wave is one tile per SM,
+// and a tile's time was measured to grow only slowly with BN (one wave of
+// INT4 tiles: 20.0 us at BN = 64, 24.3 us at 256), the per-K-step
+// dequantization of the 128-row weight tile being the fixed part C0 (in
+// token units).  Ties go to the wider tile.
+int pick_bn(int64_t M, int64_t N, int sms, int code_tile_bytes, bool allow_wide) {
   const int64_t nblk = (N + BM - 1) / BM;
-  const int64_t floor_bn = 128;
+  const int64_t c0 = 850;
   int best = 16;
   int64_t best_cost = -1;
-  for (int bn = 16; bn <= BN_MAX; bn += 16) {
+  for (int bn = 16; bn <= BN_WIDE_MAX; bn += bn < BN_MAX ? 16 : 32) {
+    // a wide tile only with a ring of at least three stages (measured: two are too shallow)
+    const int stage = BM * BK * 2 + bn * BK * 2 + code_tile_bytes;
+    if (bn > BN_MAX && (!allow_wide || (SMEM_LIMIT - 2048) / stage < 3)) break;
     const int64_t tiles = ((M + bn - 1) / bn) * nblk;
     const int64_t waves = (tiles + sms - 1) / sms;
-    const int64_t cost = waves * (bn > floor_bn ? bn : floor_bn);
+    const int64_t cost = waves * (c0 + bn);
     if (best_cost < 0 || cost <= best_cost) {
       best_cost = cost;
       best = bn;
@@ -487,7 +508,7 @@ cudaError_t launch_bits(const uint16_t *x_bf16, const uint32_t *codes, const Gem
   {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {BK, (cuuint32_t)p.bn};
+    cuuint32_t box[2] = {BK, (cuuint32_t)p.bn_sub};
     cuuint32_t es[2] = {1, 1};
     if (encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x_bf16), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -509,7 +530,9 @@ cudaError_t launch_bits(const uint16_t *x_bf16, const uint32_t *codes, const Gem
   pp.stages = S::stages(p.bn);
   if (pp.stages < 2) return cudaErrorNotSupported;
   const int alloc = S::alloc(p.bn);
-  auto kern = (p.gshift == 6 && p.coef_vec) ? qmm_gemm_kernel<BITS, true> : qmm_gemm_kernel<BITS, false>;
+  const bool g64 = p.gshift == 6 && p.coef_vec;
+  auto kern = p.nsub == 2 ? (g64 ? qmm_gemm_kernel<BITS, true, 2> : qmm_gemm_kernel<BITS, false, 2>)
+                          : (g64 ? qmm_gemm_kernel<BITS, true, 1> : qmm_gemm_kernel<BITS, false, 1>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alloc);
   if (e != cudaSuccess) return e;
   const int grid = p.tiles < sm_count_gemm() ? p.tiles : sm_count_gemm();
@@ -532,7 +555,10 @@ cudaError_t launch_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uin
   p.gshift = __builtin_ctz((unsigned)group);
   p.groups_per_row = (int)(K / group);
   p.coef_vec = (p.groups_per_row % 8 == 0) ? 1 : 0;   // rows are then 16-byte multiples (bases are 16-aligned)
-  p.bn = pick_bn(M, N, sm_count_gemm());
+  // (Q1, whose per-K-step dequantization is the lightest, measured slower with wide tiles)
+  p.bn = pick_bn(M, N, sm_count_gemm(), BM * (bits == 4 ? 32 : bits == 8 ? 64 : 16), bits != 1);
+  p.nsub = p.bn > BN_MAX ? 2 : 1;
+  p.bn_sub = p.bn / p.nsub;
   p.m_blocks = (int)((M + p.bn - 1) / p.bn);
   p.n_blocks = (int)((N + BM - 1) / BM);
   p.tiles = p.m_blocks * p.n_blocks;

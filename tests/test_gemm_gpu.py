@@ -24,8 +24,10 @@ SHAPES = [  # M, N, K, group: single and several tiles, ragged M and N, every BN
     (1, 128, 64, 64), (7, 200, 128, 64), (64, 256, 2048, 64), (100, 300, 1024, 128),
     (129, 1000, 512, 64), (256, 384, 2048, 64), (300, 130, 256, 64), (513, 1024, 2048, 64),
     (1024, 640, 1024, 128),
-    # more 128-row tiles than SMs: the 256-row tiling (ragged M and N, both group sizes)
-    (700, 7000, 1024, 64), (513, 5000, 512, 128),
+    # more tiles than SMs (ragged M and N, both group sizes); the first and the last two take token
+    # tiles wider than 256 (two MMAs per k-slice into one accumulator), the last with a ragged
+    # second half
+    (700, 7000, 1024, 64), (513, 5000, 512, 128), (1000, 6144, 128, 64), (300, 19456, 128, 64),
 ]
 
 
@@ -46,6 +48,7 @@ def test_small_shapes(qmm, oracle_mod, M, N, K, group):
 FORMATS = [  # M, N, K, bits, group: INT8 and Q1 codes through the same tensor-core pipeline
     (1, 128, 128, 8, 64), (100, 300, 1024, 8, 128), (513, 1024, 2048, 8, 64), (700, 7000, 1024, 8, 64),
     (1, 128, 128, 1, 128), (129, 1000, 512, 1, 64), (300, 130, 256, 1, 128), (1024, 2048, 5120, 1, 128),
+    (1000, 6144, 256, 1, 128),   # Q1 where INT4 and INT8 would take token tiles wider than 256
 ]
 
 
