@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), 128);
+      mbar_init(acc_empty(b), NSUB == 1 ? 128 : 128 + DQ_THREADS);   // wide: the dequantization warps help
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -173,6 +173,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // The y rows of a finished accumulator: this warp's TMEM lane quarter, the
+  // 32-column chunks c with c % nroles == role (one role per epilogue warp; a
+  // wide tile's single accumulator is shared with the dequantization warps).
+  auto store_tile = [&](int tile, int buf, int role, int nroles) {
+    const int q = warp & 3;                          // TMEM lane quarter this warp may read
+    const int r = q * 32 + lane;                     // weight row within the tile
+    const int mb = tile % p.m_blocks, nb = tile / p.m_blocks;
+    tc_fence_after();
+    const int n = nb * BM + r;
+    const int m0 = mb * bn;
+    const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN_MAX;
+#pragma unroll 1
+    for (int c0 = 32 * role; c0 < bn; c0 += 32 * nroles) {
+      if (c0 + 32 <= bn) {
+        uint32_t v[32];
+        __syncwarp();                  // tcgen05.ld is .sync.aligned: the whole warp, converged
+        tmem_ld_32x32b_x32(tbase + c0, v);
+        tmem_ld_wait();
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; j++) {
+            const int m = m0 + c0 + j;
+            if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
+          }
+        }
+      } else {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_32x32b_x16(tbase + c0, v);
+        tmem_ld_wait();
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 16; j++) {
+            const int m = m0 + c0 + j;
+            if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
+          }
+        }
+      }
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -269,6 +310,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = t >> 1, part = t & 1;             // weight row within the tile, k half
     const int G = p.groups_per_row;
     Ring ring;
+    int dq_local = 0;         // tiles of this CTA so far
     bool ok = true;
     bool ready = false;       // the current stage seen complete by a test issued one K-step early
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
@@ -382,51 +424,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ring.next(STAGES);
       }
       }
+      if constexpr (NSUB == 2) {
+        // a wide tile's accumulator is the only one: help drain it
+        if (!ok) break;
+        if (!__all_sync(0xffffffffu, wait_bounded(acc_full(0), dq_local & 1, ctl))) { ok = false; break; }
+        store_tile(tile, 0, 1 + (warp - DQ_WARP0) / 4, 3);
+        tc_fence_before();
+        mbar_arrive(acc_empty(0));
+      }
+      dq_local++;
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                          // TMEM lane quarter this warp may read
-    const int r = q * 32 + lane;                     // weight row within the tile
     int local = 0;
     bool ok = true;
     constexpr int nbuf = NSUB == 1 ? 2 : 1;
     for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, local++) {
-      const int mb = tile % p.m_blocks, nb = tile / p.m_blocks;
       const int buf = local % nbuf;
       const uint32_t use = (local / nbuf) & 1;
       if (!__all_sync(0xffffffffu, wait_bounded(acc_full(buf), use, ctl))) { ok = false; break; }
-      tc_fence_after();
-      const int n = nb * BM + r;
-      const int m0 = mb * bn;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN_MAX;
-#pragma unroll 1
-      for (int c0 = 0; c0 < bn; c0 += 32) {
-        if (c0 + 32 <= bn) {
-          uint32_t v[32];
-          __syncwarp();                  // tcgen05.ld is .sync.aligned: the whole warp, converged
-          tmem_ld_32x32b_x32(tbase + c0, v);
-          tmem_ld_wait();
-          if (n < p.N) {
-#pragma unroll
-            for (int j = 0; j < 32; j++) {
-              const int m = m0 + c0 + j;
-              if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
-            }
-          }
-        } else {
-          uint32_t v[16];
-          __syncwarp();
-          tmem_ld_32x32b_x16(tbase + c0, v);
-          tmem_ld_wait();
-          if (n < p.N) {
-#pragma unroll
-            for (int j = 0; j < 16; j++) {
-              const int m = m0 + c0 + j;
-              if (m < p.M) __stcs(p.y + (int64_t)m * p.N + n, __uint_as_float(v[j]));
-            }
-          }
-        }
-      }
+      store_tile(tile, buf, 0, NSUB == 1 ? 1 : 3);
       tc_fence_before();
       mbar_arrive(acc_empty(buf));
     }
