@@ -499,6 +499,8 @@ int pick_bn(int64_t M, int64_t N, int sms, int code_tile_bytes, bool allow_wide)
     // a wide tile only with a ring of at least three stages (measured: two are too shallow)
     const int stage = BM * BK * 2 + bn * BK * 2 + code_tile_bytes;
     if (bn > BN_MAX && (!allow_wide || (SMEM_LIMIT - 2048) / stage < 3)) break;
+    // the last token tile of a wide width must reach into its second x box
+    if (bn > BN_MAX && M - ((M + bn - 1) / bn - 1) * bn <= bn / 2) continue;
     const int64_t tiles = ((M + bn - 1) / bn) * nblk;
     const int64_t waves = (tiles + sms - 1) / sms;
     const int64_t cost = waves * (c0 + bn);
