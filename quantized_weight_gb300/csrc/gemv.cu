@@ -398,12 +398,17 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
     cudaError_t e = launch_gemv_q1(x, codes, scales, y, N, K, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
+  if (M >= 2 && M <= 4 && bits == 8) {
+    // INT8, 2-4 tokens: the streamed kernel unpacks each code once for all of them
+    cudaError_t e = launch_gemv_stream(x, codes, scales, biases, y, M, N, K, bits, group, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (M >= 2) {
     cudaError_t e = launch_gemv_batch(x, codes, scales, biases, y, M, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
   if (M == 1) {
-    cudaError_t e = launch_gemv_stream(x, codes, scales, biases, y, N, K, bits, group, s);
+    cudaError_t e = launch_gemv_stream(x, codes, scales, biases, y, 1, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
   if (bits == 4) return launch_bits<4>(p, s);

@@ -90,6 +90,7 @@ struct StreamParams {
   // shared-memory layout (bytes from the 128-byte-aligned base)
   int off_coef, off_x, off_red, off_bar, off_am;
   ArgmaxWork am;       // used by the argmax epilogue only
+  int M;               // tokens: 1, or 2..4 for INT8
 };
 
 // INT4, two rows at once; see the file comment.  x pairs per word:
@@ -148,6 +149,41 @@ __device__ __forceinline__ float dot_int8(const uint4 c, const f2 (&xp)[8]) {
   f2_split(a0, c0, c1);
   f2_split(a1, c2, c3);
   return (c0 + c1) + (c2 + c3);
+}
+
+// INT8, tokens 0 .. NQ: each code word unpacked once, multiplied into every
+// token's activations (token 0 in xp, tokens 1 .. NQ in xq).
+template <int NQ>
+__device__ __forceinline__ void dot_int8_mt(const uint4 c, const f2 (&xp)[8], const f2 (&xq)[NQ][8], float &d0,
+                                            float (&dq)[NQ]) {
+  const f2 off2 = f2_make(8388736.0f, 8388736.0f);     // 2^23 + 128
+  f2 a0 = f2_zero(), a1 = f2_zero(), b0[NQ], b1[NQ];
+#pragma unroll
+  for (int m = 0; m < NQ; m++) b0[m] = f2_zero(), b1[m] = f2_zero();
+  const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int wi = 0; wi < 4; wi++) {
+    const uint32_t w = wv[wi] ^ 0x80808080u;
+    const f2 q01 = f2_sub(f2_bits(prmt(w, kMagic, 0x7540u), prmt(w, kMagic, 0x7541u)), off2);
+    const f2 q23 = f2_sub(f2_bits(prmt(w, kMagic, 0x7542u), prmt(w, kMagic, 0x7543u)), off2);
+    a0 = f2_fma(q01, xp[2 * wi + 0], a0);
+    a1 = f2_fma(q23, xp[2 * wi + 1], a1);
+#pragma unroll
+    for (int m = 0; m < NQ; m++) {
+      b0[m] = f2_fma(q01, xq[m][2 * wi + 0], b0[m]);
+      b1[m] = f2_fma(q23, xq[m][2 * wi + 1], b1[m]);
+    }
+  }
+  float c0, c1, c2, c3;
+  f2_split(a0, c0, c1);
+  f2_split(a1, c2, c3);
+  d0 = (c0 + c1) + (c2 + c3);
+#pragma unroll
+  for (int m = 0; m < NQ; m++) {
+    f2_split(b0[m], c0, c1);
+    f2_split(b1[m], c2, c3);
+    dq[m] = (c0 + c1) + (c2 + c3);
+  }
 }
 
 __device__ __forceinline__ float dot_q1(const uint32_t w, const f2 (&xp)[16]) {
@@ -222,8 +258,13 @@ __device__ __forceinline__ void stage_x(const float *__restrict__ x, int K, f2 *
 // copied with its codes (a whole slab's coefficients would crowd out the
 // ring).  Otherwise: up to 15 consumer warps, two CTAs per SM where they fit,
 // the slab's coefficients copied once.
-template <int BITS, bool ARGMAX, bool WIDE>
-__global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_kernel(const StreamParams p) {
+// MT (INT8 only): tokens per launch, each code unpacked once for all of them;
+// the extra activation registers leave room for one CTA per SM.
+template <int BITS, bool ARGMAX, bool WIDE, int MT>
+__global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
+    gemv_stream_kernel(const StreamParams p) {
+  static_assert(MT == 1 || (BITS == 8 && !ARGMAX && !WIDE), "several tokens: INT8 products only");
+  constexpr int NQ = MT > 1 ? MT - 1 : 1;                        // tokens after the first (array extent)
   using L = Lane<BITS>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = p.stages;
@@ -233,7 +274,7 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
   const uint16_t *sc = reinterpret_cast<const uint16_t *>(smem + p.off_coef);
   const uint16_t *bi = sc + p.rows_per_cta * p.G;
   f2 *xs = reinterpret_cast<f2 *>(smem + p.off_x);                 // [segs][PAIRS][32 lanes]
-  float *red = reinterpret_cast<float *>(smem + p.off_red);        // [rows_per_cta][segs]
+  float *red = reinterpret_cast<float *>(smem + p.off_red);        // [rows_per_cta][segs][MT]
   const uint32_t bars = sbase + p.off_bar;
   auto full = [&](int s) { return bars + 8 * s; };
   auto empty = [&](int s) { return bars + 8 * (S + s); };
@@ -335,6 +376,7 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
   }
   pdl_wait();                                                    // x is written by the previous kernel
   f2 xp[L::PAIRS];
+  f2 xq[NQ][L::PAIRS];                                           // tokens 1 .. MT-1 (MT > 1 only)
   if constexpr (BITS == 8) {
     // INT8: this lane's 16 activations (64 contiguous bytes), loaded
     // straight into its register pairs (measured faster than staging)
@@ -344,6 +386,19 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
       const float4 v = ld_nc_f4(src + 4 * i);
       xp[2 * i] = f2_make(v.x, v.y);
       xp[2 * i + 1] = f2_make(v.z, v.w);
+    }
+    if constexpr (MT > 1) {
+      // the other tokens; past M the last one repeats (its sums are not stored)
+#pragma unroll
+      for (int m = 0; m < NQ; m++) {
+        const float *sq = p.x + (int64_t)min(m + 1, p.M - 1) * p.K + seg * L::SEG_W + lane * L::W;
+#pragma unroll
+        for (int i = 0; i < L::W / 4; i++) {
+          const float4 v = ld_nc_f4(sq + 4 * i);
+          xq[m][2 * i] = f2_make(v.x, v.y);
+          xq[m][2 * i + 1] = f2_make(v.z, v.w);
+        }
+      }
     }
   } else {
     // INT4: x once per CTA, coalesced, staged in shared memory as each lane's
@@ -402,6 +457,7 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
       crow = rbase - j * p.stage_rows;
     }
     float part[RG];
+    float partq[RG][NQ];                                         // tokens 1 .. MT-1 (MT > 1 only)
     if constexpr (BITS == 4) {
 #pragma unroll
       for (int rr = 0; rr < RG; rr += 2) {
@@ -419,7 +475,13 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
         const int r = rr < nr ? rr : 0;
         const uint8_t *cp = st + r * p.row_bytes + lane_off;
         const float sv = h2f(scg[(crow + r) * p.G + g]);
-        if constexpr (BITS == 8) {
+        if constexpr (BITS == 8 && MT > 1) {
+          float d0, dq[NQ];
+          dot_int8_mt<NQ>(*reinterpret_cast<const uint4 *>(cp), xp, xq, d0, dq);
+          part[rr] = sv * d0;
+#pragma unroll
+          for (int m = 0; m < NQ; m++) partq[rr][m] = sv * dq[m];
+        } else if constexpr (BITS == 8) {
           part[rr] = sv * dot_int8(*reinterpret_cast<const uint4 *>(cp), xp);
         } else {
           part[rr] = sv * dot_q1(*reinterpret_cast<const uint32_t *>(cp), xp);
@@ -442,7 +504,24 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
     k += __shfl_xor_sync(0xffffffffu, k, 2);
     k += __shfl_xor_sync(0xffffffffu, k, 1);
     const int rr = (h16 ? 2 : 0) + (h8 ? 1 : 0);
-    if ((lane & 7) == 0 && rr < nr) red[(rbase + rr) * p.segs + seg] = k;
+    if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * MT] = k;
+    if constexpr (MT > 1) {
+      // the same butterfly for the other tokens
+#pragma unroll
+      for (int m = 0; m < NQ; m++) {
+        float q0 = h16 ? partq[2][m] : partq[0][m], q1 = h16 ? partq[3][m] : partq[1][m];
+        const float t0 = h16 ? partq[0][m] : partq[2][m], t1 = h16 ? partq[1][m] : partq[3][m];
+        q0 += __shfl_xor_sync(0xffffffffu, t0, 16);
+        q1 += __shfl_xor_sync(0xffffffffu, t1, 16);
+        float kq = h8 ? q1 : q0;
+        const float tk = h8 ? q0 : q1;
+        kq += __shfl_xor_sync(0xffffffffu, tk, 8);
+        kq += __shfl_xor_sync(0xffffffffu, kq, 4);
+        kq += __shfl_xor_sync(0xffffffffu, kq, 2);
+        kq += __shfl_xor_sync(0xffffffffu, kq, 1);
+        if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * MT + 1 + m] = kq;
+      }
+    }
   }
   // every consumer warp gets here (the loop above only ends or breaks), so
   // the named barrier completes; after it, one thread per row adds the
@@ -465,10 +544,20 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, WIDE ? 1 : 2) gemv_stream_k
     return;
   }
   if (!fin) return;
-  for (int r = ct; r < rows; r += nthreads) {
-    float acc = 0.0f;
-    for (int q = 0; q < p.segs; q++) acc += red[r * p.segs + q];
-    p.y[n_begin + r] = acc;
+  if constexpr (MT == 1) {
+    for (int r = ct; r < rows; r += nthreads) {
+      float acc = 0.0f;
+      for (int q = 0; q < p.segs; q++) acc += red[r * p.segs + q];
+      p.y[n_begin + r] = acc;
+    }
+  } else {
+    for (int idx = ct; idx < rows * MT; idx += nthreads) {
+      const int r = idx / MT, m = idx - r * MT;
+      if (m >= p.M) continue;
+      float acc = 0.0f;
+      for (int q = 0; q < p.segs; q++) acc += red[(r * p.segs + q) * MT + m];
+      p.y[(int64_t)m * p.N + n_begin + r] = acc;
+    }
   }
 }
 
@@ -499,13 +588,15 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   if (grid > sm_count_stream()) grid = sm_count_stream();
   p.rows_per_cta = (int)((N + grid - 1) / grid);            // the largest slab of the even split
   p.wide = p.rows_per_cta > kWideRows ? 1 : 0;
+  if (p.wide && p.M > 1) return false;                          // 32 warps leave too few registers for several tokens
   const int max_warps = p.wide ? kMaxConsumerWarpsWide : kMaxConsumerWarps;
   if (p.segs > max_warps) return false;
   const int coef_row = G * 2 * (BITS == 4 ? 2 : 1);              // coefficient bytes per row
   const int coef = p.wide ? 0 : p.rows_per_cta * coef_row;      // the slab's, copied once
   const int srow = p.row_bytes + (p.wide ? coef_row : 0);        // ring bytes per row
   const int xbytes = BITS == 8 ? 0 : (int)K * 4;               // INT8 loads x into registers
-  const int redb = p.rows_per_cta * p.segs * 4;
+  const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;              // tokens per launch of the kernel
+  const int redb = p.rows_per_cta * p.segs * 4 * mt;
   const int fixed = coef + xbytes + redb + 8 * 64 + kAmScratch;
   int stage_rows0 = STAGE_ROWS_MAX;
   while (stage_rows0 > RG && stage_rows0 / 2 >= p.rows_per_cta) stage_rows0 /= 2;
@@ -546,9 +637,9 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   return true;
 }
 
-template <int BITS, bool ARGMAX, bool WIDE>
+template <int BITS, bool ARGMAX, bool WIDE, int MT = 1>
 cudaError_t launch_stream_as(const StreamParams &p0, int grid, int threads, size_t smem, cudaStream_t s) {
-  auto kern = gemv_stream_kernel<BITS, ARGMAX, WIDE>;
+  auto kern = gemv_stream_kernel<BITS, ARGMAX, WIDE, MT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // Every instantiation asks for the same (largest) shared-memory carveout, so
@@ -571,6 +662,12 @@ cudaError_t launch_stream_as(const StreamParams &p0, int grid, int threads, size
 
 template <int BITS, bool ARGMAX>
 cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t smem, cudaStream_t s) {
+  if constexpr (BITS == 8 && !ARGMAX) {
+    if (p0.M > 1) {   // (plan() keeps several tokens out of the wide layout)
+      if (p0.M <= 2) return launch_stream_as<BITS, ARGMAX, false, 2>(p0, grid, threads, smem, s);
+      return launch_stream_as<BITS, ARGMAX, false, 4>(p0, grid, threads, smem, s);
+    }
+  }
   return p0.wide ? launch_stream_as<BITS, ARGMAX, true>(p0, grid, threads, smem, s)
                  : launch_stream_as<BITS, ARGMAX, false>(p0, grid, threads, smem, s);
 }
@@ -582,9 +679,11 @@ cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t 
 // coefficient rows not 16-byte multiples, or a slab too large for shared
 // memory); the caller then uses the register-fed kernel.
 cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint16_t *scales,
-                               const uint16_t *biases, float *y, int64_t N, int64_t K, int bits, int group,
+                               const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits, int group,
                                cudaStream_t s) {
+  if (M < 1 || M > 4 || (M > 1 && bits != 8)) return cudaErrorNotSupported;
   StreamParams p{};
+  p.M = M;
   p.x = x;
   p.codes = reinterpret_cast<const uint8_t *>(codes);
   p.scales = scales;
@@ -610,6 +709,7 @@ cudaError_t launch_gemv_stream_argmax(const float *x, const uint32_t *codes, con
   p.scales = scales;
   p.biases = biases;
   p.y = nullptr;
+  p.M = 1;
   p.am = w;
   int grid = 0, threads = 0;
   size_t smem = 0;

@@ -39,11 +39,12 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
                         const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits,
                         int group, cudaStream_t s);
 
-// Decode product for M == 1 streamed through shared memory by bulk copies;
-// returns cudaErrorNotSupported (nothing launched) for shapes outside its layout.
+// Decode product for M == 1 (any format) or 2 <= M <= 4 (INT8) streamed
+// through shared memory by bulk copies; returns cudaErrorNotSupported
+// (nothing launched) for shapes outside its layout.
 cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint16_t *scales,
-                               const uint16_t *biases, float *y, int64_t N, int64_t K, int bits, int group,
-                               cudaStream_t s);
+                               const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits,
+                               int group, cudaStream_t s);
 
 // M == 1 decode product whose epilogue keeps only the argmax of y (no y is
 // written); cudaErrorNotSupported (nothing launched) outside the streaming layout.
