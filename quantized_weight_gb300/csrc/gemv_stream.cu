@@ -90,7 +90,8 @@ struct StreamParams {
   // shared-memory layout (bytes from the 128-byte-aligned base)
   int off_coef, off_x, off_red, off_bar, off_am;
   ArgmaxWork am;       // used by the argmax epilogue only
-  int M;               // tokens: 1, or 2..4 for INT8
+  int M;               // tokens: 1, or 2..8 for INT8
+  int red_tokens;      // token slots of the partial sums: MT per pass (all tokens, a pass of MT at a time)
 };
 
 // INT4, two rows at once; see the file comment.  x pairs per word:
@@ -375,12 +376,18 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
     }
   }
   pdl_wait();                                                    // x is written by the previous kernel
+  // INT8 with more tokens than MT: passes of MT tokens over the same resident
+  // slab (plan() then keeps every stage of the slab in shared memory at once)
+  const int npass = MT == 4 ? p.red_tokens / MT : 1;           // (two tokens never take a second pass)
+  const int rtok = MT == 4 ? p.red_tokens : MT;                  // token slots per partial-sum row
+  for (int pass = 0; pass < npass; pass++) {
+  const int tok0 = pass * MT;                                    // first token of the pass
   f2 xp[L::PAIRS];
   f2 xq[NQ][L::PAIRS];                                           // tokens 1 .. MT-1 (MT > 1 only)
   if constexpr (BITS == 8) {
     // INT8: this lane's 16 activations (64 contiguous bytes), loaded
     // straight into its register pairs (measured faster than staging)
-    const float *src = p.x + seg * L::SEG_W + lane * L::W;
+    const float *src = p.x + (int64_t)(MT == 1 ? 0 : min(tok0, p.M - 1)) * p.K + seg * L::SEG_W + lane * L::W;
 #pragma unroll
     for (int i = 0; i < L::W / 4; i++) {
       const float4 v = ld_nc_f4(src + 4 * i);
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
       // the other tokens; past M the last one repeats (its sums are not stored)
 #pragma unroll
       for (int m = 0; m < NQ; m++) {
-        const float *sq = p.x + (int64_t)min(m + 1, p.M - 1) * p.K + seg * L::SEG_W + lane * L::W;
+        const float *sq = p.x + (int64_t)min(tok0 + m + 1, p.M - 1) * p.K + seg * L::SEG_W + lane * L::W;
 #pragma unroll
         for (int i = 0; i < L::W / 4; i++) {
           const float4 v = ld_nc_f4(sq + 4 * i);
@@ -421,7 +428,7 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
   }
   const int g = (seg * L::SEG_W + lane * L::W) >> p.gshift;    // a lane chunk lies in one group
   const int lane_off = seg * L::SEG_BYTES + lane * L::BYTES;
-  if (!p.two_per_sm) ok = __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
+  if (!p.two_per_sm && pass == 0) ok = ok && __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
 
   // the group's stage j, ring slot s and phase ph (where a warp walks many
   // groups, a wide slab or INT8 with one warp per segment, they advance
@@ -489,7 +496,7 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty(s));                        // this group's codes are consumed
+    if (lane == 0 && pass + 1 == npass) mbar_arrive(empty(s));  // this group's codes are consumed
     // transposing butterfly: 4 row partials over 32 lanes in 6 shuffles;
     // afterwards lane l holds the warp total of row 2*bit4(l) + bit3(l)
     const bool h16 = lane & 16, h8 = lane & 8;
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
     k += __shfl_xor_sync(0xffffffffu, k, 2);
     k += __shfl_xor_sync(0xffffffffu, k, 1);
     const int rr = (h16 ? 2 : 0) + (h8 ? 1 : 0);
-    if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * MT] = k;
+    if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * rtok + tok0] = k;
     if constexpr (MT > 1) {
       // the same butterfly for the other tokens
 #pragma unroll
@@ -519,9 +526,11 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
         kq += __shfl_xor_sync(0xffffffffu, kq, 4);
         kq += __shfl_xor_sync(0xffffffffu, kq, 2);
         kq += __shfl_xor_sync(0xffffffffu, kq, 1);
-        if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * MT + 1 + m] = kq;
+        if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * rtok + tok0 + 1 + m] = kq;
       }
     }
+  }
+  prewaited = 0x7FFFFFFF;                                        // a later pass finds every stage waited for
   }
   // every consumer warp gets here (the loop above only ends or breaks), so
   // the named barrier completes; after it, one thread per row adds the
@@ -551,11 +560,12 @@ __global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
       p.y[n_begin + r] = acc;
     }
   } else {
-    for (int idx = ct; idx < rows * MT; idx += nthreads) {
-      const int r = idx / MT, m = idx - r * MT;
+    const int rt = rtok;
+    for (int idx = ct; idx < rows * rt; idx += nthreads) {
+      const int r = idx / rt, m = idx - r * rt;
       if (m >= p.M) continue;
       float acc = 0.0f;
-      for (int q = 0; q < p.segs; q++) acc += red[(r * p.segs + q) * MT + m];
+      for (int q = 0; q < p.segs; q++) acc += red[(r * p.segs + q) * rt + m];
       p.y[(int64_t)m * p.N + n_begin + r] = acc;
     }
   }
@@ -595,8 +605,10 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   const int coef = p.wide ? 0 : p.rows_per_cta * coef_row;      // the slab's, copied once
   const int srow = p.row_bytes + (p.wide ? coef_row : 0);        // ring bytes per row
   const int xbytes = BITS == 8 ? 0 : (int)K * 4;               // INT8 loads x into registers
-  const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;              // tokens per launch of the kernel
-  const int redb = p.rows_per_cta * p.segs * 4 * mt;
+  const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;              // tokens per pass
+  const int npass = (p.M + mt - 1) / mt;
+  p.red_tokens = mt * npass;
+  const int redb = p.rows_per_cta * p.segs * 4 * p.red_tokens;
   const int fixed = coef + xbytes + redb + 8 * 64 + kAmScratch;
   int stage_rows0 = STAGE_ROWS_MAX;
   while (stage_rows0 > RG && stage_rows0 / 2 >= p.rows_per_cta) stage_rows0 /= 2;
@@ -605,7 +617,7 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
   // long as it keeps two stages in flight; else the deepest ring that fits.
   // A wide slab takes the deepest ring that fits.
   int S = 0;
-  for (int sr = stage_rows0; !p.wide && sr >= RG && S == 0; sr /= 2) {
+  for (int sr = stage_rows0; !p.wide && npass == 1 && sr >= RG && S == 0; sr /= 2) {
     const int nst = (p.rows_per_cta + sr - 1) / sr;
     int s2 = (kSmemPair - fixed) / (sr * srow);
     if (s2 > nst) s2 = nst;
@@ -618,6 +630,7 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
     if (S > nst) S = nst;
   }
   if (S < 1) return false;
+  if (npass > 1 && S < (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows) return false;   // the slab must stay resident
   const int stage_bytes = p.stage_rows * srow;
   p.stage_bytes = stage_bytes;
   p.stages = S;
@@ -681,7 +694,7 @@ cudaError_t launch_stream(const StreamParams &p0, int grid, int threads, size_t 
 cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint16_t *scales,
                                const uint16_t *biases, float *y, int M, int64_t N, int64_t K, int bits, int group,
                                cudaStream_t s) {
-  if (M < 1 || M > 4 || (M > 1 && bits != 8)) return cudaErrorNotSupported;
+  if (M < 1 || M > 8 || (M > 1 && bits != 8)) return cudaErrorNotSupported;
   StreamParams p{};
   p.M = M;
   p.x = x;
