@@ -22,7 +22,8 @@
 //               rounding; INT8 s*q and Q1 +-s, exact), then round-to-nearest-
 //               even bf16, stored swizzled, proxy-fenced; the row's scales
 //               (and biases) come eight groups at a time with 16-byte loads,
-//               one chunk ahead
+//               one chunk ahead (group 64: K-steps eight at a time, unrolled);
+//               with wide tiles they also help drain the accumulator
 //   warps 10-13 epilogue: tcgen05.ld of the f32 accumulator, y stored with
 //               32 consecutive n per warp-wide store
 //
@@ -35,9 +36,9 @@
 // wider tiles are two MMAs per k-slice (two x boxes of BN/2 rows) into one
 // accumulator of BN columns, which dequantizes each weight tile for more
 // tokens: on the M = 1024 shapes one wave of 3 x 48 tiles instead of two
-// waves of 6 x 48.  Stage
-// buffers are guarded by mbarriers (TMA -> full, dequant -> afull,
-// MMA commit -> empty).
+// waves of 6 x 48.  Stage buffers (as many as shared memory holds, up to
+// eight) are guarded by mbarriers (TMA -> full, dequant -> afull, MMA commit
+// -> empty).
 //
 // Every wait is bounded by wall time (bounded_wait.cuh).  A wait that runs out
 // records QMM_ERR_DEVICE_TIMEOUT in a device status word, raises a CTA-wide
