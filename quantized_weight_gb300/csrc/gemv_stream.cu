@@ -59,7 +59,7 @@ constexpr int kSmemBudget = 200 * 1024;
 constexpr int kSmemPair = 108 * 1024;      // leaves room for two CTAs per SM
 constexpr int kAmScratch = 8 * 32;         // argmax scratch: two words per consumer warp
 constexpr int kMaxConsumerWarps = 15;
-constexpr int kMaxConsumerWarpsWide = 31;  // long slabs: one CTA per SM, 32 warps
+constexpr int kMaxConsumerWarpsWide = 27;  // long slabs: one CTA per SM, 28 warps
 constexpr int kWideRows = 128;             // slabs longer than this take the wide layout
 
 template <int BITS>
@@ -254,15 +254,15 @@ __device__ __forceinline__ void stage_x(const float *__restrict__ x, int K, f2 *
   }
 }
 
-// WIDE (slabs longer than kWideRows rows, e.g. a vocabulary head): up to 31
-// consumer warps, a deep ring, and the coefficients of each stage's rows
+// WIDE (slabs longer than kWideRows rows, e.g. a vocabulary head): up to 27
+// consumer warps (72 registers each: measured faster than 31 at 64), a deep ring, and the coefficients of each stage's rows
 // copied with its codes (a whole slab's coefficients would crowd out the
 // ring).  Otherwise: up to 15 consumer warps, two CTAs per SM where they fit,
 // the slab's coefficients copied once.
 // MT (INT8 only): tokens per launch, each code unpacked once for all of them;
 // the extra activation registers leave room for one CTA per SM.
 template <int BITS, bool ARGMAX, bool WIDE, int MT>
-__global__ void __launch_bounds__(WIDE ? 1024 : 512, (WIDE || MT > 1) ? 1 : 2)
+__global__ void __launch_bounds__(WIDE ? 896 : 512, (WIDE || MT > 1) ? 1 : 2)
     gemv_stream_kernel(const StreamParams p) {
   static_assert(MT == 1 || (BITS == 8 && !ARGMAX && !WIDE), "several tokens: INT8 products only");
   constexpr int NQ = MT > 1 ? MT - 1 : 1;                        // tokens after the first (array extent)
