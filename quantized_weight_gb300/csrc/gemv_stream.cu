@@ -255,12 +255,14 @@ __device__ __forceinline__ void stage_x(const float *__restrict__ x, int K, f2 *
 }
 
 // WIDE (slabs longer than kWideRows rows, e.g. a vocabulary head): up to 27
-// consumer warps (72 registers each: measured faster than 31 at 64), a deep ring, and the coefficients of each stage's rows
-// copied with its codes (a whole slab's coefficients would crowd out the
-// ring).  Otherwise: up to 15 consumer warps, two CTAs per SM where they fit,
-// the slab's coefficients copied once.
-// MT (INT8 only): tokens per launch, each code unpacked once for all of them;
-// the extra activation registers leave room for one CTA per SM.
+// consumer warps (72 registers each: measured faster than 31 at 64), a deep
+// ring, and the coefficients of each stage's rows copied with its codes (a
+// whole slab's coefficients would crowd out the ring).  Otherwise: up to 15
+// consumer warps, two CTAs per SM where they fit, the slab's coefficients
+// copied once.
+// MT (INT8 only): tokens per pass, each code unpacked once for all of them
+// (more tokens: passes over a slab kept resident); the extra activation
+// registers leave room for one CTA per SM.
 template <int BITS, bool ARGMAX, bool WIDE, int MT>
 __global__ void __launch_bounds__(WIDE ? 896 : 512, (WIDE || MT > 1) ? 1 : 2)
     gemv_stream_kernel(const StreamParams p) {
@@ -381,156 +383,156 @@ __global__ void __launch_bounds__(WIDE ? 896 : 512, (WIDE || MT > 1) ? 1 : 2)
   const int npass = MT == 4 ? p.red_tokens / MT : 1;           // (two tokens never take a second pass)
   const int rtok = MT == 4 ? p.red_tokens : MT;                  // token slots per partial-sum row
   for (int pass = 0; pass < npass; pass++) {
-  const int tok0 = pass * MT;                                    // first token of the pass
-  f2 xp[L::PAIRS];
-  f2 xq[NQ][L::PAIRS];                                           // tokens 1 .. MT-1 (MT > 1 only)
-  if constexpr (BITS == 8) {
-    // INT8: this lane's 16 activations (64 contiguous bytes), loaded
-    // straight into its register pairs (measured faster than staging)
-    const float *src = p.x + (int64_t)(MT == 1 ? 0 : min(tok0, p.M - 1)) * p.K + seg * L::SEG_W + lane * L::W;
+    const int tok0 = pass * MT;                                    // first token of the pass
+    f2 xp[L::PAIRS];
+    f2 xq[NQ][L::PAIRS];                                           // tokens 1 .. MT-1 (MT > 1 only)
+    if constexpr (BITS == 8) {
+      // INT8: this lane's 16 activations (64 contiguous bytes), loaded
+      // straight into its register pairs (measured faster than staging)
+      const float *src = p.x + (int64_t)(MT == 1 ? 0 : min(tok0, p.M - 1)) * p.K + seg * L::SEG_W + lane * L::W;
 #pragma unroll
-    for (int i = 0; i < L::W / 4; i++) {
-      const float4 v = ld_nc_f4(src + 4 * i);
-      xp[2 * i] = f2_make(v.x, v.y);
-      xp[2 * i + 1] = f2_make(v.z, v.w);
-    }
-    if constexpr (MT > 1) {
-      // the other tokens; past M the last one repeats (its sums are not stored)
-#pragma unroll
-      for (int m = 0; m < NQ; m++) {
-        const float *sq = p.x + (int64_t)min(tok0 + m + 1, p.M - 1) * p.K + seg * L::SEG_W + lane * L::W;
-#pragma unroll
-        for (int i = 0; i < L::W / 4; i++) {
-          const float4 v = ld_nc_f4(sq + 4 * i);
-          xq[m][2 * i] = f2_make(v.x, v.y);
-          xq[m][2 * i + 1] = f2_make(v.z, v.w);
-        }
+      for (int i = 0; i < L::W / 4; i++) {
+        const float4 v = ld_nc_f4(src + 4 * i);
+        xp[2 * i] = f2_make(v.x, v.y);
+        xp[2 * i + 1] = f2_make(v.z, v.w);
       }
-    }
-  } else {
-    // INT4: x once per CTA, coalesced, staged in shared memory as each lane's
-    // register pairs (a lane's 128 contiguous bytes load slowly from L1)
-    if (p.two_per_sm) stage_x<BITS, 4>(p.x, p.K, xs, ct, nthreads);
-    else stage_x<BITS, 1>(p.x, p.K, xs, ct, nthreads);
-    // consumer warps only; every consumer thread reaches it (no exit before)
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+      if constexpr (MT > 1) {
+        // the other tokens; past M the last one repeats (its sums are not stored)
 #pragma unroll
-    for (int i = 0; i < L::PAIRS; i++) xp[i] = xs[(seg * L::PAIRS + i) * 32 + lane];
-  }
-  float xsum = 0.0f;
-  if constexpr (BITS == 4) {
+        for (int m = 0; m < NQ; m++) {
+          const float *sq = p.x + (int64_t)min(tok0 + m + 1, p.M - 1) * p.K + seg * L::SEG_W + lane * L::W;
 #pragma unroll
-    for (int i = 0; i < L::PAIRS; i++) {
-      float a, b;
-      f2_split(xp[i], a, b);
-      xsum += a + b;
-    }
-  }
-  const int g = (seg * L::SEG_W + lane * L::W) >> p.gshift;    // a lane chunk lies in one group
-  const int lane_off = seg * L::SEG_BYTES + lane * L::BYTES;
-  if (!p.two_per_sm && pass == 0) ok = ok && __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
-
-  // the group's stage j, ring slot s and phase ph (where a warp walks many
-  // groups, a wide slab or INT8 with one warp per segment, they advance
-  // without a division; measured slower for the short INT4 slabs)
-  int j = t0 / groups_per_stage, jrem = t0 - j * groups_per_stage;
-  int s = j % S;
-  uint32_t ph = (j / S) & 1;
-  for (int grp = t0; ok && grp < ngroups; grp += p.wps) {
-    if constexpr (WIDE || BITS != 4) {
-      if (grp != t0) {
-        jrem += p.wps;
-        while (jrem >= groups_per_stage) {
-          jrem -= groups_per_stage;
-          j++;
-          if (++s == S) s = 0, ph ^= 1u;
+          for (int i = 0; i < L::W / 4; i++) {
+            const float4 v = ld_nc_f4(sq + 4 * i);
+            xq[m][2 * i] = f2_make(v.x, v.y);
+            xq[m][2 * i + 1] = f2_make(v.z, v.w);
+          }
         }
       }
     } else {
-      j = grp / groups_per_stage;
-      s = j % S;
-      ph = (j / S) & 1;
+      // INT4: x once per CTA, coalesced, staged in shared memory as each lane's
+      // register pairs (a lane's 128 contiguous bytes load slowly from L1)
+      if (p.two_per_sm) stage_x<BITS, 4>(p.x, p.K, xs, ct, nthreads);
+      else stage_x<BITS, 1>(p.x, p.K, xs, ct, nthreads);
+      // consumer warps only; every consumer thread reaches it (no exit before)
+      asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+#pragma unroll
+      for (int i = 0; i < L::PAIRS; i++) xp[i] = xs[(seg * L::PAIRS + i) * 32 + lane];
     }
-    if (j > prewaited && !__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
-    const int rbase = grp * RG;                                  // first row (within the CTA)
-    const int nr = min(RG, rows - rbase);
-    const uint8_t *st = smem + s * p.stage_bytes + (rbase - j * p.stage_rows) * p.row_bytes;
-    // this group's coefficient rows: in the stage (wide layout), or in the slab
-    const uint16_t *scg = sc, *big = bi;
-    int crow = rbase;
-    if constexpr (WIDE) {
-      scg = reinterpret_cast<const uint16_t *>(smem + s * p.stage_bytes + code_stage_bytes);
-      big = scg + p.stage_rows * p.G;
-      crow = rbase - j * p.stage_rows;
-    }
-    float part[RG];
-    float partq[RG][NQ];                                         // tokens 1 .. MT-1 (MT > 1 only)
+    float xsum = 0.0f;
     if constexpr (BITS == 4) {
 #pragma unroll
-      for (int rr = 0; rr < RG; rr += 2) {
-        const int ra = rr < nr ? rr : 0, rb = rr + 1 < nr ? rr + 1 : 0;
-        float da, db;
-        dot2_int4(*reinterpret_cast<const uint4 *>(st + ra * p.row_bytes + lane_off),
-                  *reinterpret_cast<const uint4 *>(st + rb * p.row_bytes + lane_off), xp, da, db);
-        const int ia = (crow + ra) * p.G + g, ib = (crow + rb) * p.G + g;
-        part[rr] = fmaf(h2f(scg[ia]), da, h2f(big[ia]) * xsum);
-        part[rr + 1] = fmaf(h2f(scg[ib]), db, h2f(big[ib]) * xsum);
+      for (int i = 0; i < L::PAIRS; i++) {
+        float a, b;
+        f2_split(xp[i], a, b);
+        xsum += a + b;
       }
-    } else {
+    }
+    const int g = (seg * L::SEG_W + lane * L::W) >> p.gshift;    // a lane chunk lies in one group
+    const int lane_off = seg * L::SEG_BYTES + lane * L::BYTES;
+    if (!p.two_per_sm && pass == 0) ok = ok && __all_sync(0xffffffffu, wait_bounded(coef_full, 0, ctl));
+
+    // the group's stage j, ring slot s and phase ph (where a warp walks many
+    // groups, a wide slab or INT8 with one warp per segment, they advance
+    // without a division; measured slower for the short INT4 slabs)
+    int j = t0 / groups_per_stage, jrem = t0 - j * groups_per_stage;
+    int s = j % S;
+    uint32_t ph = (j / S) & 1;
+    for (int grp = t0; ok && grp < ngroups; grp += p.wps) {
+      if constexpr (WIDE || BITS != 4) {
+        if (grp != t0) {
+          jrem += p.wps;
+          while (jrem >= groups_per_stage) {
+            jrem -= groups_per_stage;
+            j++;
+            if (++s == S) s = 0, ph ^= 1u;
+          }
+        }
+      } else {
+        j = grp / groups_per_stage;
+        s = j % S;
+        ph = (j / S) & 1;
+      }
+      if (j > prewaited && !__all_sync(0xffffffffu, wait_bounded(full(s), ph, ctl))) { ok = false; break; }
+      const int rbase = grp * RG;                                  // first row (within the CTA)
+      const int nr = min(RG, rows - rbase);
+      const uint8_t *st = smem + s * p.stage_bytes + (rbase - j * p.stage_rows) * p.row_bytes;
+      // this group's coefficient rows: in the stage (wide layout), or in the slab
+      const uint16_t *scg = sc, *big = bi;
+      int crow = rbase;
+      if constexpr (WIDE) {
+        scg = reinterpret_cast<const uint16_t *>(smem + s * p.stage_bytes + code_stage_bytes);
+        big = scg + p.stage_rows * p.G;
+        crow = rbase - j * p.stage_rows;
+      }
+      float part[RG];
+      float partq[RG][NQ];                                         // tokens 1 .. MT-1 (MT > 1 only)
+      if constexpr (BITS == 4) {
 #pragma unroll
-      for (int rr = 0; rr < RG; rr++) {
-        const int r = rr < nr ? rr : 0;
-        const uint8_t *cp = st + r * p.row_bytes + lane_off;
-        const float sv = h2f(scg[(crow + r) * p.G + g]);
-        if constexpr (BITS == 8 && MT > 1) {
-          float d0, dq[NQ];
-          dot_int8_mt<NQ>(*reinterpret_cast<const uint4 *>(cp), xp, xq, d0, dq);
-          part[rr] = sv * d0;
+        for (int rr = 0; rr < RG; rr += 2) {
+          const int ra = rr < nr ? rr : 0, rb = rr + 1 < nr ? rr + 1 : 0;
+          float da, db;
+          dot2_int4(*reinterpret_cast<const uint4 *>(st + ra * p.row_bytes + lane_off),
+                    *reinterpret_cast<const uint4 *>(st + rb * p.row_bytes + lane_off), xp, da, db);
+          const int ia = (crow + ra) * p.G + g, ib = (crow + rb) * p.G + g;
+          part[rr] = fmaf(h2f(scg[ia]), da, h2f(big[ia]) * xsum);
+          part[rr + 1] = fmaf(h2f(scg[ib]), db, h2f(big[ib]) * xsum);
+        }
+      } else {
 #pragma unroll
-          for (int m = 0; m < NQ; m++) partq[rr][m] = sv * dq[m];
-        } else if constexpr (BITS == 8) {
-          part[rr] = sv * dot_int8(*reinterpret_cast<const uint4 *>(cp), xp);
-        } else {
-          part[rr] = sv * dot_q1(*reinterpret_cast<const uint32_t *>(cp), xp);
+        for (int rr = 0; rr < RG; rr++) {
+          const int r = rr < nr ? rr : 0;
+          const uint8_t *cp = st + r * p.row_bytes + lane_off;
+          const float sv = h2f(scg[(crow + r) * p.G + g]);
+          if constexpr (BITS == 8 && MT > 1) {
+            float d0, dq[NQ];
+            dot_int8_mt<NQ>(*reinterpret_cast<const uint4 *>(cp), xp, xq, d0, dq);
+            part[rr] = sv * d0;
+#pragma unroll
+            for (int m = 0; m < NQ; m++) partq[rr][m] = sv * dq[m];
+          } else if constexpr (BITS == 8) {
+            part[rr] = sv * dot_int8(*reinterpret_cast<const uint4 *>(cp), xp);
+          } else {
+            part[rr] = sv * dot_q1(*reinterpret_cast<const uint32_t *>(cp), xp);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && pass + 1 == npass) mbar_arrive(empty(s));  // this group's codes are consumed
+      // transposing butterfly: 4 row partials over 32 lanes in 6 shuffles;
+      // afterwards lane l holds the warp total of row 2*bit4(l) + bit3(l)
+      const bool h16 = lane & 16, h8 = lane & 8;
+      float k0 = h16 ? part[2] : part[0], k1 = h16 ? part[3] : part[1];
+      const float s0 = h16 ? part[0] : part[2], s1 = h16 ? part[1] : part[3];
+      k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+      k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+      float k = h8 ? k1 : k0;
+      const float sk = h8 ? k0 : k1;
+      k += __shfl_xor_sync(0xffffffffu, sk, 8);
+      k += __shfl_xor_sync(0xffffffffu, k, 4);
+      k += __shfl_xor_sync(0xffffffffu, k, 2);
+      k += __shfl_xor_sync(0xffffffffu, k, 1);
+      const int rr = (h16 ? 2 : 0) + (h8 ? 1 : 0);
+      if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * rtok + tok0] = k;
+      if constexpr (MT > 1) {
+        // the same butterfly for the other tokens
+#pragma unroll
+        for (int m = 0; m < NQ; m++) {
+          float q0 = h16 ? partq[2][m] : partq[0][m], q1 = h16 ? partq[3][m] : partq[1][m];
+          const float t0 = h16 ? partq[0][m] : partq[2][m], t1 = h16 ? partq[1][m] : partq[3][m];
+          q0 += __shfl_xor_sync(0xffffffffu, t0, 16);
+          q1 += __shfl_xor_sync(0xffffffffu, t1, 16);
+          float kq = h8 ? q1 : q0;
+          const float tk = h8 ? q0 : q1;
+          kq += __shfl_xor_sync(0xffffffffu, tk, 8);
+          kq += __shfl_xor_sync(0xffffffffu, kq, 4);
+          kq += __shfl_xor_sync(0xffffffffu, kq, 2);
+          kq += __shfl_xor_sync(0xffffffffu, kq, 1);
+          if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * rtok + tok0 + 1 + m] = kq;
         }
       }
     }
-    __syncwarp();
-    if (lane == 0 && pass + 1 == npass) mbar_arrive(empty(s));  // this group's codes are consumed
-    // transposing butterfly: 4 row partials over 32 lanes in 6 shuffles;
-    // afterwards lane l holds the warp total of row 2*bit4(l) + bit3(l)
-    const bool h16 = lane & 16, h8 = lane & 8;
-    float k0 = h16 ? part[2] : part[0], k1 = h16 ? part[3] : part[1];
-    const float s0 = h16 ? part[0] : part[2], s1 = h16 ? part[1] : part[3];
-    k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-    k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-    float k = h8 ? k1 : k0;
-    const float sk = h8 ? k0 : k1;
-    k += __shfl_xor_sync(0xffffffffu, sk, 8);
-    k += __shfl_xor_sync(0xffffffffu, k, 4);
-    k += __shfl_xor_sync(0xffffffffu, k, 2);
-    k += __shfl_xor_sync(0xffffffffu, k, 1);
-    const int rr = (h16 ? 2 : 0) + (h8 ? 1 : 0);
-    if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * rtok + tok0] = k;
-    if constexpr (MT > 1) {
-      // the same butterfly for the other tokens
-#pragma unroll
-      for (int m = 0; m < NQ; m++) {
-        float q0 = h16 ? partq[2][m] : partq[0][m], q1 = h16 ? partq[3][m] : partq[1][m];
-        const float t0 = h16 ? partq[0][m] : partq[2][m], t1 = h16 ? partq[1][m] : partq[3][m];
-        q0 += __shfl_xor_sync(0xffffffffu, t0, 16);
-        q1 += __shfl_xor_sync(0xffffffffu, t1, 16);
-        float kq = h8 ? q1 : q0;
-        const float tk = h8 ? q0 : q1;
-        kq += __shfl_xor_sync(0xffffffffu, tk, 8);
-        kq += __shfl_xor_sync(0xffffffffu, kq, 4);
-        kq += __shfl_xor_sync(0xffffffffu, kq, 2);
-        kq += __shfl_xor_sync(0xffffffffu, kq, 1);
-        if ((lane & 7) == 0 && rr < nr) red[((rbase + rr) * p.segs + seg) * rtok + tok0 + 1 + m] = kq;
-      }
-    }
-  }
-  prewaited = 0x7FFFFFFF;                                        // a later pass finds every stage waited for
+    prewaited = 0x7FFFFFFF;                                        // a later pass finds every stage waited for
   }
   // every consumer warp gets here (the loop above only ends or breaks), so
   // the named barrier completes; after it, one thread per row adds the
@@ -630,7 +632,8 @@ bool plan(int64_t N, int64_t K, int group, StreamParams &p, int &grid, int &thre
     if (S > nst) S = nst;
   }
   if (S < 1) return false;
-  if (npass > 1 && S < (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows) return false;   // the slab must stay resident
+  // several passes read the slab again: all of it must stay resident
+  if (npass > 1 && S < (p.rows_per_cta + p.stage_rows - 1) / p.stage_rows) return false;
   const int stage_bytes = p.stage_rows * srow;
   p.stage_bytes = stage_bytes;
   p.stages = S;
