@@ -160,7 +160,9 @@ BATCH = [(2, 6144, 2048, 4, 64), (4, 6144, 2048, 4, 64), (8, 2048, 6144, 4, 64),
          # INT8, 5..8 tokens in one pass: the benchmark shape, fewer rows than SMs, a ragged slab
          (8, 4096, 4096, 8, 64), (6, 150, 512, 8, 64), (7, 2333, 3072, 8, 64),
          # INT8 at the benchmark's two tokens, ragged slabs of 10-16 rows
-         (2, 4096, 4096, 8, 64), (4, 3000, 2048, 8, 64), (3, 4864, 1024, 8, 32), (6, 2500, 512, 8, 128)]
+         (2, 4096, 4096, 8, 64), (4, 3000, 2048, 8, 64), (3, 4864, 1024, 8, 32), (6, 2500, 512, 8, 128),
+         # INT8 slabs too long for the streamed kernel's token passes (wide layout): the fallbacks
+         (6, 40000, 1024, 8, 64), (2, 40000, 1024, 8, 64)]
 
 
 # M = 1 slabs whose coefficients travel with each code stage (more than 16 KB
