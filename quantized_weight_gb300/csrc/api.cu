@@ -135,7 +135,9 @@ int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scale
   if (M == 1) {
     qmm::ArgmaxWork w{reinterpret_cast<unsigned *>(ws), reinterpret_cast<float *>(ws + 16),
                       reinterpret_cast<int32_t *>(ws + 16 + 4 * qmm::kArgmaxMaxCtas), idx, val};
-    cudaError_t e = qmm::launch_gemv_stream_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
+    cudaError_t e = qmm::launch_gemv_tc_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+    e = qmm::launch_gemv_stream_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
     if (e != cudaErrorNotSupported) return cuda_status(e);
   }
   float *logits = reinterpret_cast<float *>(ws + kArgmaxHead);
@@ -171,12 +173,13 @@ int qmm_gather_dequant(const int32_t *ids, int64_t T, const uint32_t *packed, co
 
 int qmm_check(qmm_stream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return QMM_ERR_CUDA;
-  int st[4] = {0, 0, 0, 0};
+  int st[5] = {0, 0, 0, 0, 0};
   if (qmm::read_clear_gemm_status(&st[0], stream) != cudaSuccess) return QMM_ERR_CUDA;
   if (qmm::read_clear_gemv_status(&st[1], stream) != cudaSuccess) return QMM_ERR_CUDA;
   if (qmm::read_clear_q1_status(&st[2], stream) != cudaSuccess) return QMM_ERR_CUDA;
   if (qmm::read_clear_batch_status(&st[3], stream) != cudaSuccess) return QMM_ERR_CUDA;
-  return (st[0] | st[1] | st[2] | st[3]) != 0 ? QMM_ERR_DEVICE_TIMEOUT : QMM_OK;
+  if (qmm::read_clear_tc_status(&st[4], stream) != cudaSuccess) return QMM_ERR_CUDA;
+  return (st[0] | st[1] | st[2] | st[3] | st[4]) != 0 ? QMM_ERR_DEVICE_TIMEOUT : QMM_OK;
 }
 
 }  // extern "C"

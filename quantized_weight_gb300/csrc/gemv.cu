@@ -394,6 +394,11 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
   p.gshift = __builtin_ctz((unsigned)group);
   p.chunks_per_row = (int)(K * bits / 128);
   p.groups_per_row = (int)(K / group);
+  {
+    // the tensor-core kernel first; the kernels below take the shapes it does not
+    cudaError_t e = launch_gemv_tc(x, codes, scales, biases, y, M, N, K, bits, group, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (M == 1 && bits == 1) {
     cudaError_t e = launch_gemv_q1(x, codes, scales, y, N, K, group, s);
     if (e != cudaErrorNotSupported) return e;

@@ -1,0 +1,1016 @@
+// gemv_tc.cu -- decode product y[M, N] = x[M, K] * dequant(W)^T (M = 1..8) on
+// the warp-level tensor-core path (mma.sync m16n8k16, f16 inputs, f32
+// accumulation).
+//
+// Decode reads every weight once and is bound by memory bandwidth ("... Tesla
+// C2075 ..." paper, section 3.3 "Decode, and why 4-bit is slower"); what
+// decides whether a kernel reaches that bound is the instruction cost of
+// turning packed codes into products.  Here the tensor cores take the
+// multiply-add and the reduction across k, and the only per-weight work left
+// on the integer pipes is moving codes into MMA operand registers:
+//
+//   * A binary16 bit pattern whose bits 11..15 are zero is the integer it
+//     spells times 2^-24 (subnormals and the first normal binade share one
+//     spacing), and the MMA multiplies such subnormal operands exactly.  So a
+//     code masked in place is already an exact operand: INT4 nibbles at bits
+//     0..3 and 4..7 of each 16-bit half give q * 2^-24 and 16 q * 2^-24 (one
+//     AND each; one shift per word brings the other two nibbles down), INT8
+//     bytes (XOR 0x80 makes them q + 128) are spread into 16-bit halves by one
+//     byte permute, and a Q1 sign bit i of a half (i <= 10) is 2^i * 2^-24.
+//   * The k-dependent factors (1/16 for the upper nibble, 2^-i for a sign
+//     bit) are folded into the activation operand, which is built once per
+//     CTA: x of each token is scaled by a power of two 2^S (so that its largest
+//     magnitude lies in [2^14, 2^15)), split into two binary16 terms hi + lo
+//     (22 significant bits, the dropped part at most 2^-22 |x|), and stored in
+//     shared memory in the B-fragment order the MMAs read.
+//   * Each MMA gives D = 2^-24 * sum(code * x'); per (row, group) the kernel
+//     adds s * D and, once per group, the x-only correction (b * sum x' for the
+//     INT4 bias, -128 s * sum x' for the INT8 offset, -s * sum x' for Q1's
+//     w = s (2 bit - 1)), all in FP32; the sums of x' per group come from the
+//     same preparation pass.  y = total * 2^(24 - S), exactly.
+//
+// Operand layout.  A = 16 weight rows x 16 k (rows g and g + 8 of a lane's
+// quad), B = 16 k x 8 columns.  Each lane quad t = 0..3 contributes the k of
+// its own code words; a column is non-zero only at the k of the lanes whose
+// words belong to the column's group, so one MMA can keep several groups
+// apart: with one token the 8 columns are (group of lane t, hi/lo) for the
+// four lanes' four different groups, with two tokens (group pair, token,
+// hi/lo), and from three tokens on (token, hi/lo) over one group.  The D
+// registers of lane t then hold exactly the (group, token) it applies the
+// coefficients of, so the per-group epilogue costs a few FMAs per lane.
+//
+// Layout of the work.  Each CTA (one per SM, or two where a CTA's shared
+// memory allows, so that the next product's CTA streams its weights while
+// this one computes) owns a contiguous slab of up to 256 rows.  One TMA
+// tensor copy brings the slab's codes into shared memory as 128-byte columns
+// of all its rows (the 128-byte swizzle puts the eight rows one warp
+// instruction reads in eight different bank groups), and one more per
+// coefficient array brings the scales (and biases) as 8-group blocks of all
+// rows; the engine's cost is per copy, so a handful of large copies replace
+// one per row.  The copies do not depend on the previous kernel in the
+// stream, so they are issued before the programmatic-dependent-launch wait.
+// The 16 warps then take runs of (16-row tile, k-step) work.  Longer slabs (a
+// vocabulary head) stream through a ring of 16-row stages fed by a producer
+// warp, and their work units (tile, K slice) go round robin to 15 consumer
+// warps.  Partial sums land in per-(unit, row, token) shared-memory slots;
+// after a barrier one thread per output adds them in a fixed order: no
+// atomics, the same bits on every run.
+//
+// Every mbarrier wait is bounded (bounded_wait.cuh); a wait that runs out
+// aborts the CTA, drains its outstanding copies and records
+// QMM_ERR_DEVICE_TIMEOUT for qmm_check().
+#include <algorithm>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "argmax.cuh"
+#include "bounded_wait.cuh"
+#include "qmm_device.cuh"
+#include "qmm_launch.h"
+#include "sm100_ptx.cuh"
+
+namespace qmm {
+
+__device__ int g_tc_status = 0;
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 512;              // 16 warps
+constexpr int kTileRows = 16;              // rows per MMA tile and per stage
+constexpr int kSmemMax = 225 * 1024;
+constexpr int kSmemPair = 113 * 1024;      // at most this much shared memory: two CTAs per SM
+constexpr int kAmScratch = 2 * 4 * 32;
+
+// Per code format: k per 32-bit word.
+template <int FMT> struct Fmt;
+template <> struct Fmt<4> { static constexpr int WPK = 8; };
+template <> struct Fmt<8> { static constexpr int WPK = 4; };
+template <> struct Fmt<1> { static constexpr int WPK = 32; };
+
+struct TcParams {
+  const float *x;
+  float *y;
+  int M, N, K, G, NG;
+  int row_bytes, row_words;
+  int ncoef;                 // coefficient arrays (2: scales and biases; 1: scales)
+  int gpm, lg_gpm;           // groups per MMA (4, 2, 1) and its log2
+  int lg_lpg;                // log2 of the lanes per group (4 / gpm)
+  int wpg, lg_wpg;           // code words per group row
+  int wl, lg_wl;             // words per lane per group
+  int npos, spt;             // lane word positions per tile row; UW-steps per tile
+  int R;                     // rows of the largest CTA slab (not wide) or of a ring stage (wide: 16)
+  int BH;                    // rows per copy box: 8 (not wide: a slab is copied as 8-row boxes) or 16
+  int noct;                  // not wide: 8-row blocks of the N rows (split evenly over the CTAs)
+  int wide, nks, lg_nks;     // ring + round-robin units of nks K slices per tile
+  int stages;                // ring depth (1 when not wide)
+  int code_bytes;            // codes of one slab / stage: R * row_bytes (boxes of BH rows one after another)
+  int coef_bytes;            // one coefficient array of one slab / stage: R * NG * 2
+  int stage_bytes;           // slab / stage: codes, then the coefficient arrays (1024-byte multiple)
+  int warp0, nwarps;         // first consumer warp, consumer warps
+  int nj2;                   // MMA pairs per tile row (B fragments)
+  int nact0, nact1;          // active B lanes per MMA in column blocks 0 and 1
+  int pstr0, pstr1;          // bytes per MMA pair of B in column blocks 0 and 1 (16 * nact + 16)
+  int off_b, off_xs, off_red, off_zero, off_bar, off_am;
+  ArgmaxWork am;
+};
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> two binary16 (round to nearest even): low half from `lo`.
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ void f16x2_to_f32(uint32_t v, float &lo, float &hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(v));
+}
+// The pair (a, b) of activation values as two binary16 terms each:
+// hi = f16(a), f16(b); lo = f16 of the exact float residuals.
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint32_t &lo) {
+  hi = f16x2(a, b);
+  float ha, hb;
+  f16x2_to_f32(hi, ha, hb);
+  lo = f16x2(a - ha, b - hb);
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }   // -126 <= e <= 127
+
+// v * 2^e for -102 <= e <= 137, exact unless the result over- or underflows.
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+  if (e > 127) {
+    v *= pow2f(127);
+    e -= 127;
+  }
+  return v * pow2f(e);
+}
+
+// Exponent S of the activation scale 2^S from the largest |x| bit pattern:
+// max |x| * 2^S lies in [2^14, 2^15).  Zero or non-finite maxima take S = 0.
+__device__ __forceinline__ int scale_exp(uint32_t mbits) {
+  if (mbits == 0u || mbits >= 0x7F800000u) return 0;
+  const int e = (int)(mbits >> 23) - 127;
+  const int S = 14 - e;
+  return S > 126 ? 126 : S;
+}
+
+__device__ __forceinline__ uint32_t absbits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
+// Code words [word0, word0 + UW) of one row.  A copy box of BH rows holds
+// 128-byte columns of its rows (column stride BH * 128 bytes), each 16-byte
+// chunk swizzled within its 128-byte line (chunk ^= row & 7, the TMA 128-byte
+// swizzle on a 1024-byte-aligned base); `rowb` is the row's line in column 0,
+// `sw` its swizzle.  word0 is a multiple of UW.  Plain loads, so that the
+// compiler may schedule them early.
+template <int UW>
+__device__ __forceinline__ void lds_codes(const uint8_t *smem, int rowb, int colstride, int sw, int word0,
+                                          uint32_t (&w)[UW]) {
+  const uint8_t *lb = smem + (rowb + (word0 >> 5) * colstride);
+  const int ch = (word0 >> 2) & 7;
+  if constexpr (UW == 2) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(lb + ((ch ^ sw) << 4) + (word0 & 3) * 4);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < UW; i += 4) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(lb + (((ch + (i >> 2)) ^ sw) << 4));
+      w[i] = v.x;
+      w[i + 1] = v.y;
+      w[i + 2] = v.z;
+      w[i + 3] = v.w;
+    }
+  }
+}
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+__device__ __forceinline__ uint16_t lds16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
+
+// B column (and its column block) of token m's term tau for the words of lane t.
+__device__ __forceinline__ void b_lane(int gpm, int m, int t, int tau, int &cb, int &ai) {
+  if (gpm == 4) {
+    cb = 0;
+    ai = 2 * t + tau;                        // lanes (g = 2t + tau, t), index g
+  } else if (gpm == 2) {
+    cb = 0;
+    ai = 4 * t + 2 * m + tau;                // lanes (g = 4 (t / 2) + 2m + tau, t)
+  } else {
+    cb = m >> 2;
+    ai = 4 * (2 * (m & 3) + tau) + t;        // lanes (g = 2 (m % 4) + tau, t), index = lane id
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+// Not wide: with W working warps (W = min(16, steps)), warp w takes the
+// k-steps [run(w), run(w + 1)) of the slab's tiles, in (tile, k-step) order;
+// every run is non-empty.
+__host__ __device__ __forceinline__ int run_begin(int w, int W, int total) { return w * total / W; }
+// First and last of those warps whose runs include k-steps of tile `tile`.
+__host__ __device__ __forceinline__ int first_warp(int tile, int spt, int W, int total) {
+  return (W * (tile * spt + 1) + total - 1) / total - 1;
+}
+__host__ __device__ __forceinline__ int last_warp(int tile, int spt, int W, int total) {
+  return (W * ((tile + 1) * spt) + total - 1) / total - 1;
+}
+
+template <int FMT, int UW, int MT, bool ARGMAX>
+__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
+    gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+                   const __grid_constant__ CUtensorMap tm_biases, const TcParams p) {
+  using F = Fmt<FMT>;
+  // MMAs of one k-step spread over NA independent accumulators
+  constexpr int MPS = UW * (FMT == 4 ? 2 : FMT == 8 ? 1 : 8);
+  constexpr int NA = MPS < 2 ? MPS : 2;
+  // the parameters the loops use, in registers (the lambdas below capture
+  // only these locals, never the parameter block itself)
+  const int M = p.M, K = p.K, NG = p.NG, R = p.R, row_words = p.row_words;
+  const int gpm = p.gpm, lg_gpm = p.lg_gpm, lg_lpg = p.lg_lpg, wpg = p.wpg, lg_wpg = p.lg_wpg;
+  const int wl = p.wl, lg_wl = p.lg_wl, npos = p.npos, spt = p.spt;
+  const bool wide = p.wide != 0;
+  const int nks = p.nks, lg_nks = p.lg_nks, S = p.stages, stage_bytes = p.stage_bytes;
+  const int code_bytes = p.code_bytes, coef_bytes = p.coef_bytes;
+  const int nj2 = p.nj2, nact0 = p.nact0, nact1 = p.nact1, nwarps = p.nwarps, warp0 = p.warp0;
+  const int BH = p.BH, row_bytes = p.row_bytes, pstr0 = p.pstr0, pstr1 = p.pstr1;
+  const float *__restrict__ xg_in = p.x;
+
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the swizzled code columns need a 1024-byte-aligned base (the launch adds 1 KB)
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bars = sbase + p.off_bar;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_bar + 8 * (2 * S));
+  float4 *xgc = reinterpret_cast<float4 *>(smem + p.off_xs);      // [M][NG] per-(token, group) constants
+  float *red = reinterpret_cast<float *>(smem + p.off_red);
+  const int b_off = p.off_b, zero_off = p.off_zero;
+  const WaitCtl ctl{abort_flag, &g_tc_status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // not wide: R rows per CTA (the last CTA fewer); wide: the CTA's share of the rows
+  int n_begin, rows;
+  if (wide) {
+    n_begin = (int)((int64_t)blockIdx.x * p.N / gridDim.x);
+    rows = (int)((int64_t)(blockIdx.x + 1) * p.N / gridDim.x) - n_begin;
+  } else {
+    const int o0 = (int)((int64_t)blockIdx.x * p.noct / gridDim.x);
+    const int o1 = (int)((int64_t)(blockIdx.x + 1) * p.noct / gridDim.x);
+    n_begin = 8 * o0;
+    rows = min(8 * (o1 - o0), p.N - n_begin);
+  }
+  const int ntiles = (rows + kTileRows - 1) / kTileRows;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; s++) {
+      mbar_init(bars + 8 * s, 1);
+      mbar_init(bars + 8 * (S + s), nks);
+    }
+    *abort_flag = 0;
+    *reinterpret_cast<uint4 *>(smem + p.off_zero) = make_uint4(0u, 0u, 0u, 0u);   // B of inactive lanes
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  // Copies of rows [r0, r0 + R) of the slab into stage `slot`: codes as
+  // 128-byte swizzled columns, coefficients as 8-group blocks.  Rows past N
+  // are zero-filled by the copy engine.
+  const uint32_t box_bytes = (uint32_t)(BH * row_bytes + p.ncoef * BH * NG * 2);
+  if (wide) {
+    if (warp == 0) {
+      // ------------------------------------------------ producer (ring of 16-row stages)
+      if (lane == 0) {
+        const uint64_t pol = policy_evict_first();
+        bool ok = true;
+        int j = 0;
+        for (int s = 0, ph = 0; j < ntiles; j++) {
+          if (j >= S && !wait_bounded(bars + 8 * (S + s), ph ^ 1, ctl)) { ok = false; break; }
+          const uint32_t st = sbase + s * stage_bytes, fb = bars + 8 * s;
+          mbar_arrive_expect_tx(fb, box_bytes);
+          tma_load_3d_hint(st, &tm_codes, 0, n_begin + j * kTileRows, 0, fb, pol);
+          tma_load_3d_hint(st + code_bytes, &tm_scales, 0, n_begin + j * kTileRows, 0, fb, pol);
+          if (FMT == 4) tma_load_3d_hint(st + code_bytes + coef_bytes, &tm_biases, 0, n_begin + j * kTileRows, 0, fb, pol);
+          if (++s == S) s = 0, ph ^= 1;
+        }
+        if (!ok) {
+          const int first = j > S ? j - S : 0;
+          for (int i = first; i < j; i++) wait_drain(bars + 8 * (i % S), (i / S) & 1);
+        }
+      }
+      return;
+    }
+  } else if (threadIdx.x == 0) {
+    // the whole slab, resident, as 8-row boxes
+    const uint64_t pol = policy_evict_first();
+    const int nbox = (rows + 7) >> 3;
+    mbar_arrive_expect_tx(bars, (uint32_t)nbox * box_bytes);
+    for (int i = 0; i < nbox; i++) {
+      tma_load_3d_hint(sbase + i * 8 * row_bytes, &tm_codes, 0, n_begin + 8 * i, 0, bars, pol);
+      tma_load_3d_hint(sbase + code_bytes + i * 8 * NG * 2, &tm_scales, 0, n_begin + 8 * i, 0, bars, pol);
+      if (FMT == 4)
+        tma_load_3d_hint(sbase + code_bytes + coef_bytes + i * 8 * NG * 2, &tm_biases, 0, n_begin + 8 * i, 0, bars,
+                         pol);
+    }
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int cw = warp - warp0;
+  const int nthreads = nwarps * 32;
+  const int ct = cw * 32 + lane;
+  const int g = lane >> 2, t = lane & 3;
+  const int total_steps = ntiles * spt;
+  const int W = total_steps < 16 ? total_steps : 16;    // not wide: working warps
+  bool ok = true;
+  // not wide: wait for the slab before the dependent-launch wait (its copies
+  // were issued at the start; the wait overlaps the previous kernel's tail)
+  const int sb = (wide || cw >= W) ? 0 : run_begin(cw, W, total_steps);
+  const int se = (wide || cw >= W) ? 0 : run_begin(cw + 1, W, total_steps);
+  if (!wide) ok = __all_sync(0xffffffffu, wait_bounded(bars, 0, ctl));
+  pdl_wait();                                                  // x is written by the previous kernel
+
+  // ---------------------------------------------- activation preparation
+  // One pass, a thread per (token, code word), 16 floats of x per thread
+  // per round: per group g of token m the scale 2^S (largest |x| of the group
+  // in [2^14, 2^15)); x' = x * 2^S split into binary16 hi + lo and stored as
+  // B fragments; per (m, g) the constants {2^-24 sum x', f1, f2} with
+  // f1 * f2 = 2^(24 - S).  A warp's 32 words lie in one token (row_words is a
+  // multiple of 32) and a group's words in wpg adjacent lanes.
+  {
+    constexpr int NB = F::WPK >= 16 ? 1 : 16 / F::WPK;        // words per thread per round
+    const int total_words = M * row_words;
+    for (int base0 = cw * 32; base0 < total_words; base0 += NB * nthreads) {
+      float xv[NB][F::WPK];
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        const int u = base0 + b * nthreads + lane;
+        const float *src = xg_in + (int64_t)(u < total_words ? u : 0) * F::WPK;   // [M][K] = words in order
+#pragma unroll
+        for (int i = 0; i < F::WPK / 4; i++) {
+          const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
+          xv[b][4 * i] = v.x;
+          xv[b][4 * i + 1] = v.y;
+          xv[b][4 * i + 2] = v.z;
+          xv[b][4 * i + 3] = v.w;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        const int ubase = base0 + b * nthreads;
+        if (ubase >= total_words) break;                       // warp-uniform
+        const int u = ubase + lane;
+        const bool valid = u < total_words;
+        const int m = ubase / row_words;
+        const int wd = u - m * row_words;
+        // the group's largest |x|
+        uint32_t mx = 0u;
+#pragma unroll
+        for (int e = 0; e < F::WPK; e++) mx = max(mx, absbits(xv[b][e]));
+        if (!valid) mx = 0u;
+        for (int o = 1; o < wpg; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int Sx = scale_exp(mx);
+        const float sc = pow2f(Sx);
+        float wsum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < F::WPK; e++) {
+          xv[b][e] *= sc;
+          wsum += xv[b][e];
+        }
+        if (!valid) wsum = 0.0f;
+        for (int o = 1; o < wpg; o <<= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+        if (!valid) continue;
+        const int grp = wd >> lg_wpg, wig = wd & (wpg - 1);
+        if (wig == 0) {
+          const int ex = 24 - Sx, e1 = ex > 127 ? 127 : ex;
+          xgc[m * NG + grp] = make_float4(wsum * 5.9604644775390625e-08f, pow2f(e1), pow2f(ex - e1), 0.0f);
+        }
+        // this word's lane and position in the MMA sequence
+        const int gq = grp >> lg_gpm, gsel = grp & (gpm - 1);
+        const int lt = (gsel << lg_lpg) + (wig >> lg_wl);
+        const int pos = (gq << lg_wl) + (wig & (wl - 1));
+#pragma unroll
+        for (int tau = 0; tau < 2; tau++) {
+          int cb, ai;
+          b_lane(gpm, m, lt, tau, cb, ai);
+          const int pstr = cb ? pstr1 : pstr0;
+          uint8_t *bbase = smem + p.off_b + (size_t)cb * nj2 * pstr0;
+          if constexpr (FMT == 4) {
+            // MMA pair (P, Q) of this word: P (e0, e4 | e1, e5), Q (e2, e6 | e3, e7)
+            uint32_t h[4], l[4];
+            split_pair(xv[b][0], xv[b][4], h[0], l[0]);
+            split_pair(xv[b][1] * 0.0625f, xv[b][5] * 0.0625f, h[1], l[1]);
+            split_pair(xv[b][2], xv[b][6], h[2], l[2]);
+            split_pair(xv[b][3] * 0.0625f, xv[b][7] * 0.0625f, h[3], l[3]);
+            const uint32_t *v = tau ? l : h;
+            *reinterpret_cast<uint4 *>(bbase + (size_t)pos * pstr + ai * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+          } else if constexpr (FMT == 8) {
+            uint32_t h[2], l[2];
+            split_pair(xv[b][0], xv[b][1], h[0], l[0]);
+            split_pair(xv[b][2], xv[b][3], h[1], l[1]);
+            const uint32_t *v = tau ? l : h;
+            *reinterpret_cast<uint2 *>(bbase + (size_t)(pos >> 1) * pstr + ai * 16 + 8 * (pos & 1)) =
+                make_uint2(v[0], v[1]);
+          } else {
+            // MMA j of the word: (e_2j, e_16+2j | e_2j+1, e_17+2j), element e of a
+            // half at bit position e (e <= 10) or e - 11, so divided by that power
+#pragma unroll
+            for (int jp = 0; jp < 4; jp++) {
+              uint32_t v[4];
+#pragma unroll
+              for (int q = 0; q < 4; q++) {
+                const int i = 4 * jp + q;                  // register index 0..15 (= 2j or 2j + 1)
+                const float f = 1.0f / (float)(1 << (i <= 10 ? i : i - 11));
+                uint32_t hh, ll;
+                split_pair(xv[b][i] * f, xv[b][16 + i] * f, hh, ll);
+                v[q] = tau ? ll : hh;
+              }
+              *reinterpret_cast<uint4 *>(bbase + (size_t)(pos * 4 + jp) * pstr + ai * 16) =
+                  make_uint4(v[0], v[1], v[2], v[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+
+  // ---------------------------------------------------------- products
+  // B fragment addresses of this lane (inactive lanes read 16 zero bytes)
+  int baddr[MT];                   // byte offsets from the shared-memory base
+  int bstride[MT];
+  int tok[MT];
+#pragma unroll
+  for (int cb = 0; cb < MT; cb++) {
+    int active, ai;
+    if (gpm == 4) {
+      active = (g >> 1) == t;
+      ai = g;
+    } else if (gpm == 2) {
+      active = (g >> 2) == (t >> 1);
+      ai = 4 * t + (g & 3);
+    } else {
+      active = 4 * cb + (g >> 1) < M;
+      ai = 4 * g + t;
+    }
+    bstride[cb] = active ? (cb ? pstr1 : pstr0) : 0;
+    baddr[cb] = active ? b_off + cb * nj2 * pstr0 + ai * 16 : zero_off;
+    // token whose results lane t holds in column block cb
+    tok[cb] = gpm == 4 ? 0 : gpm == 2 ? (t & 1) : min(4 * cb + t, M - 1);
+  }
+  const int gsel_lane = t >> lg_lpg;                               // group of this lane within a group set
+  const int wofs_lane = (t & ((1 << lg_lpg) - 1)) << lg_wl;       // first word of this lane within its group
+
+  float acc[MT][2];
+#pragma unroll
+  for (int cb = 0; cb < MT; cb++) acc[cb][0] = acc[cb][1] = 0.0f;
+
+  // partial sums of the rows of this lane to slot `slot` (lane-quad reduction first)
+  auto flush = [&](int slot) {
+#pragma unroll
+    for (int cb = 0; cb < MT; cb++) {
+      float a0 = acc[cb][0], a1 = acc[cb][1];
+      if (gpm == 4) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, 1);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
+        a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+      } else if (gpm == 2) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
+      }
+      const bool writer = gpm == 4 ? t == 0 : gpm == 2 ? t < 2 : 4 * cb + t < M;
+      if (writer) {
+        float *dst = red + ((size_t)slot * M + tok[cb]) * kTileRows;
+        dst[g] = a0;
+        dst[g + 8] = a1;
+      }
+      acc[cb][0] = acc[cb][1] = 0.0f;
+    }
+  };
+
+  // This lane's rows ra and rb of the slab or stage at `st`: code line of
+  // column 0, swizzle, coefficient row (16-byte blocks of 8 groups, block
+  // stride BH * 16 bytes).
+  struct Rows {
+    int ca, cb, ka, kb;          // byte offsets from the shared-memory base
+    int sa, sb;
+  };
+  const int colstride = BH * 128, kblk = BH * 16;
+  auto rows_at = [&](int st, int ra, int rb) {
+    Rows q;
+    q.ca = st + (ra / BH) * BH * row_bytes + (ra % BH) * 128;
+    q.cb = st + (rb / BH) * BH * row_bytes + (rb % BH) * 128;
+    q.ka = st + code_bytes + (ra / BH) * BH * NG * 2 + (ra % BH) * 16;
+    q.kb = st + code_bytes + (rb / BH) * BH * NG * 2 + (rb % BH) * 16;
+    q.sa = ra & 7;
+    q.sb = rb & 7;
+    return q;
+  };
+
+  // One k-step (UW words per lane) at lane position pst of the rows q.
+  auto step = [&](const Rows &q, int pst) {
+    const int gq = pst >> lg_wl, wi0 = pst & (wl - 1);
+    const int grp = (gq << lg_gpm) + gsel_lane;
+    const int word0 = grp * wpg + wofs_lane + wi0;
+    const int kofs = (grp >> 3) * kblk + (grp & 7) * 2;
+    const uint8_t *ka = smem + (q.ka + kofs), *kb8 = smem + (q.kb + kofs);
+    uint32_t wa[UW], wb[UW];
+    lds_codes<UW>(smem, q.ca, colstride, q.sa, word0, wa);
+    lds_codes<UW>(smem, q.cb, colstride, q.sb, word0, wb);
+    const uint16_t sah = lds16(ka), sbh = lds16(kb8);
+    uint16_t eah = 0, ebh = 0;
+    if (FMT == 4 && wi0 == 0) {
+      eah = lds16(ka + coef_bytes);
+      ebh = lds16(kb8 + coef_bytes);
+    }
+    float4 xc[MT];
+#pragma unroll
+    for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tok[cb] * NG + grp];
+    float d[NA][MT][4];
+#pragma unroll
+    for (int a = 0; a < NA; a++)
+#pragma unroll
+      for (int cb = 0; cb < MT; cb++) d[a][cb][0] = d[a][cb][1] = d[a][cb][2] = d[a][cb][3] = 0.0f;
+#pragma unroll
+    for (int u = 0; u < UW; u++) {
+      const int pos = pst + u;
+      if constexpr (FMT == 4) {
+        const uint32_t w = wa[u], v = wb[u], w8 = w >> 8, v8 = v >> 8;
+#pragma unroll
+        for (int cb = 0; cb < MT; cb++) {
+          const uint4 b = lds128(smem + (baddr[cb] + pos * bstride[cb]));
+          mma_f16(d[(2 * u) % NA][cb], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
+          mma_f16(d[(2 * u + 1) % NA][cb], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u,
+                  b.z, b.w);
+        }
+      } else if constexpr (FMT == 8) {
+        if ((u & 1) == 0) {
+          const uint32_t w0 = wa[u] ^ 0x80808080u, v0 = wb[u] ^ 0x80808080u;
+          const uint32_t w1 = wa[u + 1] ^ 0x80808080u, v1 = wb[u + 1] ^ 0x80808080u;
+#pragma unroll
+          for (int cb = 0; cb < MT; cb++) {
+            const uint4 b = lds128(smem + (baddr[cb] + (pos >> 1) * bstride[cb]));
+            mma_f16(d[u % NA][cb], prmt(w0, 0u, 0x4140u), prmt(v0, 0u, 0x4140u), prmt(w0, 0u, 0x4342u),
+                    prmt(v0, 0u, 0x4342u), b.x, b.y);
+            mma_f16(d[(u + 1) % NA][cb], prmt(w1, 0u, 0x4140u), prmt(v1, 0u, 0x4140u), prmt(w1, 0u, 0x4342u),
+                    prmt(v1, 0u, 0x4342u), b.z, b.w);
+          }
+        }
+      } else {
+        const uint32_t w = wa[u], v = wb[u], w11 = w >> 11, v11 = v >> 11;
+#pragma unroll
+        for (int jp = 0; jp < 4; jp++) {
+          uint32_t aw[4], av[4];
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            const int i = 4 * jp + q;
+            const uint32_t mask = 0x00010001u << (i <= 10 ? i : i - 11);
+            aw[q] = (i <= 10 ? w : w11) & mask;
+            av[q] = (i <= 10 ? v : v11) & mask;
+          }
+#pragma unroll
+          for (int cb = 0; cb < MT; cb++) {
+            const uint4 b = lds128(smem + (baddr[cb] + (pos * 4 + jp) * bstride[cb]));
+            mma_f16(d[(8 * u + 2 * jp) % NA][cb], aw[0], av[0], aw[1], av[1], b.x, b.y);
+            mma_f16(d[(8 * u + 2 * jp + 1) % NA][cb], aw[2], av[2], aw[3], av[3], b.z, b.w);
+          }
+        }
+      }
+    }
+    // epilogue: (s' D + e X) * 2^(24 - S) per (row, group, token), with the
+    // x-only correction e X once per group
+    float sa = h2f(sah), sbv = h2f(sbh);
+    float ea = 0.0f, eb = 0.0f;
+    if (wi0 == 0) {
+      if constexpr (FMT == 4) {
+        ea = h2f(eah);
+        eb = h2f(ebh);
+      } else if constexpr (FMT == 8) {
+        ea = -128.0f * sa;
+        eb = -128.0f * sbv;
+      } else {
+        ea = -sa;
+        eb = -sbv;
+      }
+    }
+    if constexpr (FMT == 1) {
+      sa *= 2.0f;
+      sbv *= 2.0f;
+    }
+#pragma unroll
+    for (int cb = 0; cb < MT; cb++) {
+      float d0 = d[0][cb][0] + d[0][cb][1], d1 = d[0][cb][2] + d[0][cb][3];
+#pragma unroll
+      for (int a = 1; a < NA; a++) {
+        d0 += d[a][cb][0] + d[a][cb][1];
+        d1 += d[a][cb][2] + d[a][cb][3];
+      }
+      const float ta = fmaf(sa, d0, ea * xc[cb].x), tb = fmaf(sbv, d1, eb * xc[cb].x);
+      acc[cb][0] = fmaf(ta * xc[cb].y, xc[cb].z, acc[cb][0]);
+      acc[cb][1] = fmaf(tb * xc[cb].y, xc[cb].z, acc[cb][1]);
+    }
+  };
+
+  if (!wide) {
+    if (ok && se > sb) {
+      int tile = sb / spt, pst = (sb - tile * spt) * UW;
+      Rows q = rows_at(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
+      for (int s = sb; s < se; s++) {
+        step(q, pst);
+        pst += UW;
+        if (pst == npos || s + 1 == se) {
+          flush(cw + tile);                           // (warp, tile) -> warp + tile is one-to-one
+          pst = 0;
+          tile++;
+          q = rows_at(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
+        }
+      }
+    }
+  } else {
+    const int spu = spt >> lg_nks;                   // steps per unit
+    for (int u = cw; ok && u < ntiles * nks; u += nwarps) {
+      const int tile = u >> lg_nks, ks = u & (nks - 1);
+      const int slot = tile % S;
+      if (!__all_sync(0xffffffffu, wait_bounded(bars + 8 * slot, (tile / S) & 1, ctl))) { ok = false; break; }
+      const Rows q = rows_at(slot * stage_bytes, g, g + 8);
+      for (int s = ks * spu; s < (ks + 1) * spu; s++) step(q, s * UW);
+      flush(u);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (S + slot));
+    }
+  }
+
+  // every consumer warp gets here; then one thread per output adds the
+  // partial sums in a fixed order
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  const bool fin = ok && !*abort_flag;
+  auto total = [&](int r, int m) {
+    const int tile = r >> 4, rr = r & (kTileRows - 1);
+    float sum = 0.0f;
+    if (!wide) {
+      const int w1 = last_warp(tile, spt, W, total_steps);
+      for (int w = first_warp(tile, spt, W, total_steps); w <= w1; w++)
+        sum += red[((size_t)(w + tile) * M + m) * kTileRows + rr];
+    } else {
+      for (int ks = 0; ks < nks; ks++) sum += red[((size_t)(tile * nks + ks) * M + m) * kTileRows + rr];
+    }
+    return sum;
+  };
+  if constexpr (ARGMAX) {
+    float bv = __int_as_float(0xFF800000);
+    int bi = 0x7FFFFFFF;
+    if (fin) {
+      for (int r = ct; r < rows; r += nthreads) {
+        const float v = total(r, 0);
+        if (am_better(v, n_begin + r, bv, bi)) bv = v, bi = n_begin + r;
+      }
+    }
+    am_cta_finish(bv, bi, warp0, nwarps, reinterpret_cast<uint32_t *>(smem + p.off_am), 1, nthreads, p.am);
+    return;
+  }
+  if (!fin) return;
+  float *__restrict__ y = p.y;
+  const int N = p.N;
+  for (int idx = ct; idx < rows * M; idx += nthreads) {
+    const int m = idx / rows, r = idx - m * rows;
+    y[(int64_t)m * N + n_begin + r] = total(r, m);
+  }
+  (void)K;
+}
+
+// ---------------------------------------------------------------- host plan
+
+int sm_count_tc() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Instantiated (format, UW, MT) combinations; the greedy-argmax variants
+// mirror the plain ones (a fused argmax must sum exactly as the plain product).
+bool have_variant(int fmt, int uw, int mt) {
+  if (fmt == 4) return mt == 1 ? (uw == 2 || uw == 4 || uw == 8) : (uw == 2 || uw == 4);
+  if (fmt == 8) return uw == 4 || uw == 8;
+  return fmt == 1 && mt == 1 && uw == 2;
+}
+
+int ilog2(int v) {
+  int l = 0;
+  while ((1 << l) < v) l++;
+  return l;
+}
+
+size_t align1k(size_t v) { return (v + 1023) & ~(size_t)1023; }
+
+bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcParams &p, int &uw_out, int &grid,
+             size_t &smem) {
+  const int WPK = fmt == 4 ? 8 : fmt == 8 ? 4 : 32;
+  const int MPW = fmt == 4 ? 2 : fmt == 8 ? 1 : 8;
+  if (K % WPK != 0 || K % group != 0 || group % WPK != 0) return false;
+  const int NG = (int)(K / group);
+  if (NG % 8 != 0 || NG / 8 > 256) return false;       // coefficient rows in 16-byte blocks, one box
+  const int wpg = group / WPK;
+  const int row_words = (int)(K / WPK);
+  if (row_words % 32 != 0 || row_words / 32 > 256 || wpg > 32) return false;   // 128-byte code columns, one box
+  int gpm = 0;
+  const int cand[3] = {4, 2, 1};
+  for (int i = 0; i < 3 && !gpm; i++) {
+    const int c = cand[i];
+    if (M == 2 && c == 4) continue;
+    if (M >= 3 && c != 1) continue;
+    if (NG % c == 0 && (wpg * c) % 4 == 0) gpm = c;
+  }
+  if (!gpm) return false;
+  const int mt = M > 4 ? 2 : 1;
+  if (mt == 2 && gpm != 1) return false;
+  if (argmax && mt != 1) return false;
+  const int wl = wpg * gpm / 4;
+  const int npos = row_words / 4;
+  const int sms = sm_count_tc();
+  const int row_bytes = (int)(K * (fmt == 4 ? 4 : fmt == 8 ? 8 : 1) / 8);
+  const int ncoef = fmt == 4 ? 2 : 1;
+  int nact0, nact1 = 0;
+  if (gpm == 4) nact0 = 8;
+  else if (gpm == 2) nact0 = 16;
+  else {
+    nact0 = 8 * (M < 4 ? M : 4);
+    nact1 = M > 4 ? 8 * (M - 4) : 0;
+  }
+  const int nj2 = npos * MPW / 2;
+  // B pair stride, padded by 16 bytes (conflict-free stores in the
+  // preparation) unless that costs a slab two CTAs per SM
+  int pstr0 = nact0 * 16 + 16, pstr1 = nact1 ? nact1 * 16 + 16 : 0;
+  size_t bbytes = (size_t)nj2 * (pstr0 + pstr1);
+  const size_t xsbytes = (size_t)M * NG * 16;              // {2^-24 sum x', f1, f2} per (token, group)
+  const size_t misc = 16 + kAmScratch + 16 + 1024;        // zero block, argmax scratch, abort, alignment
+
+  // rows per CTA: the 8-row blocks of N split evenly over one CTA per SM (so
+  // that no SM holds two CTAs of one product); a slab is copied as 8-row
+  // boxes, each of whose 128-byte code columns (1 KB) and 16-byte coefficient
+  // block columns (128 B) starts on a 1024- and 128-byte boundary
+  const int noct = (int)((N + 7) / 8);
+  const int grid_nw = noct < sms ? noct : sms;
+  const int R = 8 * ((noct + grid_nw - 1) / grid_nw);
+  const int ntiles = (R + kTileRows - 1) / kTileRows;
+
+  int best_uw = 0, best_wide = 0, best_S = 1, best_nks = 1, best_spt = 0;
+  double best_cost = 1e30;
+  for (int uw = 8; uw >= 2; uw >>= 1) {
+    if (wl % uw != 0 || !have_variant(fmt, uw, mt)) continue;
+    const int spt = npos / uw;
+    const double step_cost = uw * (1.0 + 0.15 * 8 / (uw * MPW));   // relative cost of one k-step
+    // resident slab (up to 256 rows): warps take runs of k-steps
+    if (R <= 256) {
+      const size_t slab = align1k((size_t)R * row_bytes + (size_t)ncoef * R * NG * 2);
+      const size_t rest = xsbytes + (size_t)(15 + ntiles) * M * kTileRows * 4 + misc + 16;
+      if (slab + bbytes + rest > (size_t)kSmemPair && slab + (size_t)nj2 * (nact0 + nact1) * 16 + rest <= (size_t)kSmemPair) {
+        pstr0 = nact0 * 16;
+        pstr1 = nact1 * 16;
+        bbytes = (size_t)nj2 * (pstr0 + pstr1);
+      }
+      // partial sums: one slot per (warp, tile) of the runs, warp + tile
+      const size_t sm = slab + bbytes + xsbytes + (size_t)(15 + ntiles) * M * kTileRows * 4 + misc + 16;
+      if (sm <= (size_t)kSmemMax) {
+        const double cost = (double)((ntiles * spt + 15) / 16) * step_cost;
+        if (cost < best_cost) {
+          best_cost = cost, best_uw = uw, best_wide = 0, best_S = 1, best_nks = 1, best_spt = spt;
+        }
+        continue;
+      }
+    }
+    // ring of 16-row stages with a producer warp; 15 consumer warps take
+    // (tile, K slice) units round robin
+    if (mt != 1) continue;
+    const int rows_w = (int)((N + sms - 1) / sms);
+    const int nt_w = (rows_w + kTileRows - 1) / kTileRows;
+    const size_t stage = align1k((size_t)kTileRows * row_bytes + (size_t)ncoef * kTileRows * NG * 2);
+    for (int nks = 1; nks <= spt; nks <<= 1) {
+      if (spt % nks) break;
+      const int ring = std::min(15 / nks + 3, nt_w);
+      const size_t smw = (size_t)ring * stage + bbytes + xsbytes + (size_t)nt_w * nks * M * kTileRows * 4 + misc +
+                         16 * (size_t)ring;
+      if (smw > (size_t)kSmemMax) continue;
+      const double c = (double)((nt_w * nks + 14) / 15) * (spt / nks) * step_cost * 16.0 / 15.0 *
+                       ((double)nt_w / std::max(1, ntiles));
+      if (c < best_cost) {
+        best_cost = c, best_uw = uw, best_wide = 1, best_S = ring, best_nks = nks, best_spt = spt;
+      }
+      break;
+    }
+  }
+  if (!best_uw) return false;
+
+  p.M = M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.G = group;
+  p.NG = NG;
+  p.row_bytes = row_bytes;
+  p.row_words = row_words;
+  p.ncoef = ncoef;
+  p.gpm = gpm;
+  p.lg_gpm = ilog2(gpm);
+  p.lg_lpg = ilog2(4 / gpm);
+  p.wpg = wpg;
+  p.lg_wpg = ilog2(wpg);
+  p.wl = wl;
+  p.lg_wl = ilog2(wl);
+  p.npos = npos;
+  p.spt = best_spt;
+  p.wide = best_wide;
+  p.nks = best_nks;
+  p.lg_nks = ilog2(best_nks);
+  p.stages = best_S;
+  p.R = best_wide ? kTileRows : R;
+  p.BH = best_wide ? kTileRows : 8;
+  p.noct = noct;
+  p.code_bytes = p.R * row_bytes;
+  p.coef_bytes = p.R * NG * 2;
+  p.stage_bytes = (int)align1k((size_t)p.code_bytes + (size_t)ncoef * p.coef_bytes);
+  p.warp0 = best_wide ? 1 : 0;
+  p.nwarps = best_wide ? 15 : 16;
+  p.nj2 = nj2;
+  p.nact0 = nact0;
+  p.nact1 = nact1;
+  p.pstr0 = pstr0;
+  p.pstr1 = pstr1;
+  if (best_wide) grid = sms < (N + 7) / 8 ? sms : (int)((N + 7) / 8);
+  else grid = grid_nw;
+  const int nt_red = best_wide ? (int)((N + grid - 1) / grid + kTileRows - 1) / kTileRows : ntiles;
+  size_t off = (size_t)p.stages * p.stage_bytes;
+  p.off_b = (int)off;
+  off += bbytes;
+  p.off_xs = (int)off;
+  off += xsbytes;
+  p.off_red = (int)off;
+  off += (best_wide ? (size_t)nt_red * best_nks : (size_t)(15 + ntiles)) * M * kTileRows * 4;
+  p.off_zero = (int)off;
+  off += 16;
+  p.off_bar = (int)off;
+  off += 8 * 2 * p.stages + 16;
+  off = (off + 15) & ~(size_t)15;
+  p.off_am = (int)off;
+  off += kAmScratch;
+  smem = off + 1024;                                       // room to align the base to 1024 bytes
+  if (smem > (size_t)kSmemMax) return false;
+  uw_out = best_uw;
+  return true;
+}
+
+// Tensor maps of the codes (128-byte columns of R rows, 128-byte swizzle)
+// and of one coefficient array (8-group blocks of R rows).
+bool encode_maps(const TcParams &p, const void *codes, const void *scales, const void *biases, CUtensorMap &tc,
+                 CUtensorMap &ts, CUtensorMap &tb) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tc_encode();
+  if (!enc) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  {
+    cuuint64_t dims[3] = {32, (cuuint64_t)p.N, (cuuint64_t)(p.row_words / 32)};
+    cuuint64_t strides[2] = {(cuuint64_t)p.row_bytes, 128};
+    cuuint32_t box[3] = {32, (cuuint32_t)p.BH, (cuuint32_t)(p.row_words / 32)};
+    if (enc(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(codes), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  cuuint64_t dims[3] = {8, (cuuint64_t)p.N, (cuuint64_t)(p.NG / 8)};
+  cuuint64_t strides[2] = {(cuuint64_t)p.NG * 2, 16};
+  cuuint32_t box[3] = {8, (cuuint32_t)p.BH, (cuuint32_t)(p.NG / 8)};
+  if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(scales), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  if (!biases) {
+    tb = ts;
+    return true;
+  }
+  return enc(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(biases), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, int UW, int MT, bool ARGMAX>
+cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUtensorMap &tb, const TcParams &p,
+                         int grid, size_t smem, cudaStream_t s) {
+  auto kern = gemv_tc_kernel<FMT, UW, MT, ARGMAX>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tc, ts, tb, p);
+}
+
+template <bool ARGMAX>
+cudaError_t launch_tc(int fmt, int uw, int mt, const CUtensorMap &tc, const CUtensorMap &ts, const CUtensorMap &tb,
+                      const TcParams &p, int grid, size_t smem, cudaStream_t s) {
+  if (fmt == 4) {
+    if (mt == 1) {
+      if (uw == 8) return launch_tc_as<4, 8, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+      if (uw == 4) return launch_tc_as<4, 4, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+      if (uw == 2) return launch_tc_as<4, 2, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+    } else if constexpr (!ARGMAX) {
+      if (uw == 4) return launch_tc_as<4, 4, 2, false>(tc, ts, tb, p, grid, smem, s);
+      if (uw == 2) return launch_tc_as<4, 2, 2, false>(tc, ts, tb, p, grid, smem, s);
+    }
+  } else if (fmt == 8) {
+    if (mt == 1) {
+      if (uw == 8) return launch_tc_as<8, 8, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+      if (uw == 4) return launch_tc_as<8, 4, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+    } else if constexpr (!ARGMAX) {
+      if (uw == 8) return launch_tc_as<8, 8, 2, false>(tc, ts, tb, p, grid, smem, s);
+      if (uw == 4) return launch_tc_as<8, 4, 2, false>(tc, ts, tb, p, grid, smem, s);
+    }
+  } else if (fmt == 1 && mt == 1 && uw == 2) {
+    return launch_tc_as<1, 2, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                           float *y, int M, int64_t N, int64_t K, int bits, int group, cudaStream_t s) {
+  if (M < 1 || M > 8) return cudaErrorNotSupported;
+  TcParams p{};
+  int uw = 0, grid = 0;
+  size_t smem = 0;
+  if (!plan_tc(bits, M, N, K, group, false, p, uw, grid, smem)) return cudaErrorNotSupported;
+  CUtensorMap tc, ts, tb;
+  if (!encode_maps(p, codes, scales, biases, tc, ts, tb)) return cudaErrorNotSupported;
+  p.x = x;
+  p.y = y;
+  return launch_tc<false>(bits, uw, M > 4 ? 2 : 1, tc, ts, tb, p, grid, smem, s);
+}
+
+cudaError_t launch_gemv_tc_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
+                                  const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
+                                  const ArgmaxWork &w, cudaStream_t s) {
+  TcParams p{};
+  int uw = 0, grid = 0;
+  size_t smem = 0;
+  if (!plan_tc(bits, 1, N, K, group, true, p, uw, grid, smem) || grid > kArgmaxMaxCtas) return cudaErrorNotSupported;
+  CUtensorMap tc, ts, tb;
+  if (!encode_maps(p, codes, scales, biases, tc, ts, tb)) return cudaErrorNotSupported;
+  p.x = x;
+  p.y = nullptr;
+  p.am = w;
+  return launch_tc<true>(bits, uw, 1, tc, ts, tb, p, grid, smem, s);
+}
+
+cudaError_t read_clear_tc_status(int *status, cudaStream_t s) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_tc_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_tc_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+  }
+  *status = v;
+  return cudaSuccess;
+}
+
+}  // namespace qmm

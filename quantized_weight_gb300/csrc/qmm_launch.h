@@ -54,6 +54,17 @@ cudaError_t launch_gemv_stream_argmax(const float *x, const uint32_t *codes, con
 // Per row m < M of logits [M, N]: idx[m] = argmax (NaN first, ties to the lower index), val[m] its value.
 cudaError_t launch_argmax_rows(const float *logits, int M, int64_t N, int32_t *idx, float *val, cudaStream_t s);
 
+// Decode product on the warp-level tensor cores (mma.sync), 1 <= M <= 8, every
+// format; returns cudaErrorNotSupported (nothing launched) for shapes outside
+// its layout (groups per row not a multiple of 8, or a lane split the
+// instantiated kernels do not cover).
+cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                           float *y, int M, int64_t N, int64_t K, int bits, int group, cudaStream_t s);
+// The same for M == 1 with the greedy-argmax epilogue (no y written).
+cudaError_t launch_gemv_tc_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
+                                  const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
+                                  const ArgmaxWork &w, cudaStream_t s);
+
 // Binary (Q1) decode product for M == 1 through per-chunk lookup tables;
 // returns cudaErrorNotSupported (nothing launched) for shapes outside its layout.
 cudaError_t launch_gemv_q1(const float *x, const uint32_t *codes, const uint16_t *scales, float *y, int64_t N,
@@ -78,5 +89,6 @@ cudaError_t read_clear_gemm_status(int *status, cudaStream_t s);
 cudaError_t read_clear_gemv_status(int *status, cudaStream_t s);
 cudaError_t read_clear_q1_status(int *status, cudaStream_t s);
 cudaError_t read_clear_batch_status(int *status, cudaStream_t s);
+cudaError_t read_clear_tc_status(int *status, cudaStream_t s);
 
 }  // namespace qmm

@@ -100,6 +100,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
       : "memory");
 }
 
+// 3-D tiled load of the box at (c0, c1, c2) with an L2 cache policy (e.g.
+// evict-first for data read once); completion as transaction bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, int32_t c0, int32_t c1, int32_t c2,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM + tcgen05
 
 // Executed by one full warp; writes the allocated TMEM base address to `slot`.
