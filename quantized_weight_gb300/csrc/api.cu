@@ -135,9 +135,7 @@ int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scale
   if (M == 1) {
     qmm::ArgmaxWork w{reinterpret_cast<unsigned *>(ws), reinterpret_cast<float *>(ws + 16),
                       reinterpret_cast<int32_t *>(ws + 16 + 4 * qmm::kArgmaxMaxCtas), idx, val};
-    cudaError_t e = qmm::launch_gemv_tc_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
-    if (e != cudaErrorNotSupported) return cuda_status(e);
-    e = qmm::launch_gemv_stream_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
+    cudaError_t e = qmm::launch_gemv_argmax_fused(x, codes, scales, biases, N, K, bits, group, w, stream);
     if (e != cudaErrorNotSupported) return cuda_status(e);
   }
   float *logits = reinterpret_cast<float *>(ws + kArgmaxHead);

@@ -394,8 +394,8 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
   p.gshift = __builtin_ctz((unsigned)group);
   p.chunks_per_row = (int)(K * bits / 128);
   p.groups_per_row = (int)(K / group);
-  {
-    // the tensor-core kernel first; the kernels below take the shapes it does not
+  if (bits == 4) {
+    // INT4: the tensor-core kernel first (measured faster for every shape it takes)
     cudaError_t e = launch_gemv_tc(x, codes, scales, biases, y, M, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
@@ -416,9 +416,27 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
     cudaError_t e = launch_gemv_stream(x, codes, scales, biases, y, 1, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
+  if (bits != 4) {
+    // INT8 / Q1 shapes the kernels above do not take
+    cudaError_t e = launch_gemv_tc(x, codes, scales, biases, y, M, N, K, bits, group, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (bits == 4) return launch_bits<4>(p, s);
   if (bits == 8) return launch_bits<8>(p, s);
   return launch_bits<1>(p, s);
+}
+
+cudaError_t launch_gemv_argmax_fused(const float *x, const uint32_t *codes, const uint16_t *scales,
+                                     const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
+                                     const ArgmaxWork &w, cudaStream_t s) {
+  // the same kernel order as launch_gemv for one token
+  if (bits == 4) {
+    const cudaError_t e = launch_gemv_tc_argmax(x, codes, scales, biases, N, K, bits, group, w, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  cudaError_t e = launch_gemv_stream_argmax(x, codes, scales, biases, N, K, bits, group, w, s);
+  if (e != cudaErrorNotSupported) return e;
+  return launch_gemv_tc_argmax(x, codes, scales, biases, N, K, bits, group, w, s);
 }
 
 }  // namespace qmm

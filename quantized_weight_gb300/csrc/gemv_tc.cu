@@ -114,7 +114,7 @@ struct TcParams {
   int nj2;                   // MMA pairs per tile row (B fragments)
   int nact0, nact1;          // active B lanes per MMA in column blocks 0 and 1
   int pstr0, pstr1;          // bytes per MMA pair of B in column blocks 0 and 1 (16 * nact + 16)
-  int off_b, off_xs, off_red, off_zero, off_bar, off_am;
+  int off_b, off_xs, off_red, off_zero, off_bar, off_am, off_tw;
   ArgmaxWork am;
 };
 
@@ -126,6 +126,15 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same with C = 0 (the first MMA of an accumulator chain).
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 // Two floats -> two binary16 (round to nearest even): low half from `lo`.
@@ -227,39 +236,41 @@ __host__ __device__ __forceinline__ int last_warp(int tile, int spt, int W, int 
   return (W * ((tile + 1) * spt) + total - 1) / total - 1;
 }
 
-template <int FMT, int UW, int MT, bool ARGMAX>
+template <int FMT, int UW, int MT, int GPM, bool ARGMAX>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_biases, const TcParams p) {
   using F = Fmt<FMT>;
-  // MMAs of one k-step spread over NA independent accumulators
-  constexpr int MPS = UW * (FMT == 4 ? 2 : FMT == 8 ? 1 : 8);
-  constexpr int NA = MPS < 2 ? MPS : 2;
-  // the parameters the loops use, in registers (the lambdas below capture
-  // only these locals, never the parameter block itself)
-  const int M = p.M, K = p.K, NG = p.NG, R = p.R, row_words = p.row_words;
-  const int gpm = p.gpm, lg_gpm = p.lg_gpm, lg_lpg = p.lg_lpg, wpg = p.wpg, lg_wpg = p.lg_wpg;
-  const int wl = p.wl, lg_wl = p.lg_wl, npos = p.npos, spt = p.spt;
+  constexpr int LPG = 4 / GPM;                     // lanes per group
+  constexpr int LG_LPG = LPG == 4 ? 2 : LPG == 2 ? 1 : 0;
+  constexpr int LG_GPM = GPM == 4 ? 2 : GPM == 2 ? 1 : 0;
+  // MMA pairs per code word (INT4: the word's P and Q MMAs; INT8: half a
+  // pair; Q1: four pairs), counted in quarter pairs
+  constexpr int QPW = FMT == 4 ? 4 : FMT == 8 ? 2 : 16;
+  // the parameters the loops use, in registers
+  const int M = p.M, NG = p.NG, row_words = p.row_words;
+  const int wpg = p.wpg, lg_wpg = p.lg_wpg, wl = p.wl, lg_wl = p.lg_wl, npos = p.npos, spt = p.spt;
   const bool wide = p.wide != 0;
   const int nks = p.nks, lg_nks = p.lg_nks, S = p.stages, stage_bytes = p.stage_bytes;
   const int code_bytes = p.code_bytes, coef_bytes = p.coef_bytes;
-  const int nj2 = p.nj2, nact0 = p.nact0, nact1 = p.nact1, nwarps = p.nwarps, warp0 = p.warp0;
-  const int BH = p.BH, row_bytes = p.row_bytes, pstr0 = p.pstr0, pstr1 = p.pstr1;
-  const float *__restrict__ xg_in = p.x;
+  const int nj2 = p.nj2, nwarps = p.nwarps, warp0 = p.warp0;
+  const int BH = p.BH, lg_bh = BH == 16 ? 4 : 3, row_bytes = p.row_bytes, pstr0 = p.pstr0, pstr1 = p.pstr1;
 
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  // the swizzled code columns need a 1024-byte-aligned base (the launch adds 1 KB)
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // the swizzled code columns need a 1024-byte-aligned base (the launch adds
+  // 1 KB); pointer arithmetic keeps the shared address space visible
+  const uint32_t sraw = smem_addr(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (sraw & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bars = sbase + p.off_bar;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_bar + 8 * (2 * S));
-  float4 *xgc = reinterpret_cast<float4 *>(smem + p.off_xs);      // [M][NG] per-(token, group) constants
+  const float4 *xgc = reinterpret_cast<const float4 *>(smem + p.off_xs);   // [M][NG] per-(token, group) constants
+  int *tw = reinterpret_cast<int *>(smem + p.off_tw);                       // not wide: [tile] first and last warp
   float *red = reinterpret_cast<float *>(smem + p.off_red);
-  const int b_off = p.off_b, zero_off = p.off_zero;
   const WaitCtl ctl{abort_flag, &g_tc_status};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // not wide: R rows per CTA (the last CTA fewer); wide: the CTA's share of the rows
+  // not wide: 8-row blocks split over the CTAs; wide: the CTA's share of the rows
   int n_begin, rows;
   if (wide) {
     n_begin = (int)((int64_t)blockIdx.x * p.N / gridDim.x);
@@ -284,9 +295,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   __syncthreads();
   pdl_launch_dependents();
 
-  // Copies of rows [r0, r0 + R) of the slab into stage `slot`: codes as
-  // 128-byte swizzled columns, coefficients as 8-group blocks.  Rows past N
-  // are zero-filled by the copy engine.
+  // Copies: codes as 128-byte swizzled columns, coefficients as 8-group
+  // blocks, one box of BH rows each; rows past N are zero-filled.
   const uint32_t box_bytes = (uint32_t)(BH * row_bytes + p.ncoef * BH * NG * 2);
   if (wide) {
     if (warp == 0) {
@@ -350,15 +360,16 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   {
     constexpr int NB = F::WPK >= 16 ? 1 : 16 / F::WPK;        // words per thread per round
     const int total_words = M * row_words;
+    float4 *xgw = reinterpret_cast<float4 *>(smem + p.off_xs);
     for (int base0 = cw * 32; base0 < total_words; base0 += NB * nthreads) {
       float xv[NB][F::WPK];
 #pragma unroll
       for (int b = 0; b < NB; b++) {
         const int u = base0 + b * nthreads + lane;
-        const float *src = xg_in + (int64_t)(u < total_words ? u : 0) * F::WPK;   // [M][K] = words in order
+        const float4 *src = reinterpret_cast<const float4 *>(p.x) + (int64_t)(u < total_words ? u : 0) * (F::WPK / 4);
 #pragma unroll
         for (int i = 0; i < F::WPK / 4; i++) {
-          const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
+          const float4 v = __ldg(src + i);
           xv[b][4 * i] = v.x;
           xv[b][4 * i + 1] = v.y;
           xv[b][4 * i + 2] = v.z;
@@ -393,18 +404,18 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         const int grp = wd >> lg_wpg, wig = wd & (wpg - 1);
         if (wig == 0) {
           const int ex = 24 - Sx, e1 = ex > 127 ? 127 : ex;
-          xgc[m * NG + grp] = make_float4(wsum * 5.9604644775390625e-08f, pow2f(e1), pow2f(ex - e1), 0.0f);
+          xgw[m * NG + grp] = make_float4(wsum * 5.9604644775390625e-08f, pow2f(e1), pow2f(ex - e1), 0.0f);
         }
         // this word's lane and position in the MMA sequence
-        const int gq = grp >> lg_gpm, gsel = grp & (gpm - 1);
-        const int lt = (gsel << lg_lpg) + (wig >> lg_wl);
+        const int gq = grp >> LG_GPM, gsel = grp & (GPM - 1);
+        const int lt = (gsel << LG_LPG) + (wig >> lg_wl);
         const int pos = (gq << lg_wl) + (wig & (wl - 1));
 #pragma unroll
         for (int tau = 0; tau < 2; tau++) {
           int cb, ai;
-          b_lane(gpm, m, lt, tau, cb, ai);
+          b_lane(GPM, m, lt, tau, cb, ai);
           const int pstr = cb ? pstr1 : pstr0;
-          uint8_t *bbase = smem + p.off_b + (size_t)cb * nj2 * pstr0;
+          uint8_t *bbase = smem + p.off_b + cb * nj2 * pstr0;
           if constexpr (FMT == 4) {
             // MMA pair (P, Q) of this word: P (e0, e4 | e1, e5), Q (e2, e6 | e3, e7)
             uint32_t h[4], l[4];
@@ -413,14 +424,13 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
             split_pair(xv[b][2], xv[b][6], h[2], l[2]);
             split_pair(xv[b][3] * 0.0625f, xv[b][7] * 0.0625f, h[3], l[3]);
             const uint32_t *v = tau ? l : h;
-            *reinterpret_cast<uint4 *>(bbase + (size_t)pos * pstr + ai * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<uint4 *>(bbase + pos * pstr + ai * 16) = make_uint4(v[0], v[1], v[2], v[3]);
           } else if constexpr (FMT == 8) {
             uint32_t h[2], l[2];
             split_pair(xv[b][0], xv[b][1], h[0], l[0]);
             split_pair(xv[b][2], xv[b][3], h[1], l[1]);
             const uint32_t *v = tau ? l : h;
-            *reinterpret_cast<uint2 *>(bbase + (size_t)(pos >> 1) * pstr + ai * 16 + 8 * (pos & 1)) =
-                make_uint2(v[0], v[1]);
+            *reinterpret_cast<uint2 *>(bbase + (pos >> 1) * pstr + ai * 16 + 8 * (pos & 1)) = make_uint2(v[0], v[1]);
           } else {
             // MMA j of the word: (e_2j, e_16+2j | e_2j+1, e_17+2j), element e of a
             // half at bit position e (e <= 10) or e - 11, so divided by that power
@@ -435,8 +445,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
                 split_pair(xv[b][i] * f, xv[b][16 + i] * f, hh, ll);
                 v[q] = tau ? ll : hh;
               }
-              *reinterpret_cast<uint4 *>(bbase + (size_t)(pos * 4 + jp) * pstr + ai * 16) =
-                  make_uint4(v[0], v[1], v[2], v[3]);
+              *reinterpret_cast<uint4 *>(bbase + (pos * 4 + jp) * pstr + ai * 16) = make_uint4(v[0], v[1], v[2], v[3]);
             }
           }
         }
@@ -446,52 +455,53 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 
   // ---------------------------------------------------------- products
-  // B fragment addresses of this lane (inactive lanes read 16 zero bytes)
-  int baddr[MT];                   // byte offsets from the shared-memory base
-  int bstride[MT];
-  int tok[MT];
+  // B fragments of this lane: byte offset and stride per MMA pair (inactive
+  // lanes read 16 zero bytes)
+  int bofs0[MT], bstr[MT], tokofs[MT], tokv[MT];
 #pragma unroll
   for (int cb = 0; cb < MT; cb++) {
     int active, ai;
-    if (gpm == 4) {
+    if constexpr (GPM == 4) {
       active = (g >> 1) == t;
       ai = g;
-    } else if (gpm == 2) {
+    } else if constexpr (GPM == 2) {
       active = (g >> 2) == (t >> 1);
       ai = 4 * t + (g & 3);
     } else {
       active = 4 * cb + (g >> 1) < M;
       ai = 4 * g + t;
     }
-    bstride[cb] = active ? (cb ? pstr1 : pstr0) : 0;
-    baddr[cb] = active ? b_off + cb * nj2 * pstr0 + ai * 16 : zero_off;
+    bstr[cb] = active ? (cb ? pstr1 : pstr0) : 0;
+    bofs0[cb] = active ? p.off_b + cb * nj2 * pstr0 + ai * 16 : p.off_zero;
     // token whose results lane t holds in column block cb
-    tok[cb] = gpm == 4 ? 0 : gpm == 2 ? (t & 1) : min(4 * cb + t, M - 1);
+    tokv[cb] = GPM == 4 ? 0 : GPM == 2 ? (t & 1) : min(4 * cb + t, M - 1);
+    tokofs[cb] = tokv[cb] * NG;
   }
-  const int gsel_lane = t >> lg_lpg;                               // group of this lane within a group set
-  const int wofs_lane = (t & ((1 << lg_lpg) - 1)) << lg_wl;       // first word of this lane within its group
+  const int gsel_lane = t >> LG_LPG;                               // group of this lane within a group set
+  const int wofs_lane = (t & (LPG - 1)) << lg_wl;                  // first word of this lane within its group
+  const int colstride = BH * 128, kblk = BH * 16;
 
   float acc[MT][2];
 #pragma unroll
   for (int cb = 0; cb < MT; cb++) acc[cb][0] = acc[cb][1] = 0.0f;
 
-  // partial sums of the rows of this lane to slot `slot` (lane-quad reduction first)
+  // partial sums of this lane's rows to slot `slot` (lane-quad reduction first)
   auto flush = [&](int slot) {
 #pragma unroll
     for (int cb = 0; cb < MT; cb++) {
       float a0 = acc[cb][0], a1 = acc[cb][1];
-      if (gpm == 4) {
+      if constexpr (GPM == 4) {
         a0 += __shfl_xor_sync(0xffffffffu, a0, 1);
         a1 += __shfl_xor_sync(0xffffffffu, a1, 1);
         a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
         a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
-      } else if (gpm == 2) {
+      } else if constexpr (GPM == 2) {
         a0 += __shfl_xor_sync(0xffffffffu, a0, 2);
         a1 += __shfl_xor_sync(0xffffffffu, a1, 2);
       }
-      const bool writer = gpm == 4 ? t == 0 : gpm == 2 ? t < 2 : 4 * cb + t < M;
+      const bool writer = GPM == 4 ? t == 0 : GPM == 2 ? t < 2 : 4 * cb + t < M;
       if (writer) {
-        float *dst = red + ((size_t)slot * M + tok[cb]) * kTileRows;
+        float *dst = red + (slot * M + tokv[cb]) * kTileRows;
         dst[g] = a0;
         dst[g + 8] = a1;
       }
@@ -499,60 +509,61 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     }
   };
 
-  // This lane's rows ra and rb of the slab or stage at `st`: code line of
-  // column 0, swizzle, coefficient row (16-byte blocks of 8 groups, block
-  // stride BH * 16 bytes).
-  struct Rows {
-    int ca, cb, ka, kb;          // byte offsets from the shared-memory base
-    int sa, sb;
-  };
-  const int colstride = BH * 128, kblk = BH * 16;
-  auto rows_at = [&](int st, int ra, int rb) {
-    Rows q;
-    q.ca = st + (ra / BH) * BH * row_bytes + (ra % BH) * 128;
-    q.cb = st + (rb / BH) * BH * row_bytes + (rb % BH) * 128;
-    q.ka = st + code_bytes + (ra / BH) * BH * NG * 2 + (ra % BH) * 16;
-    q.kb = st + code_bytes + (rb / BH) * BH * NG * 2 + (rb % BH) * 16;
-    q.sa = ra & 7;
-    q.sb = rb & 7;
-    return q;
+  // Per-tile row state of this lane: code line of column 0 and swizzle of
+  // rows ra and rb, coefficient rows (16-byte blocks of 8 groups, block
+  // stride BH * 16 bytes); byte offsets from the shared-memory base.
+  int ca = 0, cb8 = 0, swa = 0, swb = 0, ka = 0, kb8 = 0;
+  const int box_code = BH * row_bytes, box_coef = BH * NG * 2;
+  auto set_rows = [&](int st, int ra, int rb) {
+    ca = st + (ra >> lg_bh) * box_code + (ra & (BH - 1)) * 128;
+    cb8 = st + (rb >> lg_bh) * box_code + (rb & (BH - 1)) * 128;
+    ka = st + code_bytes + (ra >> lg_bh) * box_coef + (ra & (BH - 1)) * 16;
+    kb8 = st + code_bytes + (rb >> lg_bh) * box_coef + (rb & (BH - 1)) * 16;
+    swa = ra & 7;
+    swb = rb & 7;
   };
 
-  // One k-step (UW words per lane) at lane position pst of the rows q.
-  auto step = [&](const Rows &q, int pst) {
-    const int gq = pst >> lg_wl, wi0 = pst & (wl - 1);
-    const int grp = (gq << lg_gpm) + gsel_lane;
-    const int word0 = grp * wpg + wofs_lane + wi0;
-    const int kofs = (grp >> 3) * kblk + (grp & 7) * 2;
-    const uint8_t *ka = smem + (q.ka + kofs), *kb8 = smem + (q.kb + kofs);
+  // B fragments of the UW words at lane position pst: one 16-byte quarter of
+  // an MMA pair per quad (INT4: a word's P and Q; INT8: two words; Q1: a
+  // quarter of a word), for each column block.
+  constexpr int NQ = FMT == 4 ? UW : FMT == 8 ? UW / 2 : 4 * UW;
+  auto load_b = [&](int pst, uint4 (&bf)[MT][NQ]) {
+    const int q0 = FMT == 4 ? pst : FMT == 8 ? (pst >> 1) : 4 * pst;
+#pragma unroll
+    for (int cb = 0; cb < MT; cb++)
+#pragma unroll
+      for (int q = 0; q < NQ; q++) bf[cb][q] = lds128(smem + bofs0[cb] + (q0 + q) * bstr[cb]);
+  };
+
+  // One k-step: UW words per lane starting at word0 of group grp (first:
+  // word0 is the lane's first word of the group), with B fragments bf and
+  // the group's constants xc, into acc.
+  auto step = [&](int word0, int grp, bool first, const uint4 (&bf)[MT][NQ], const float4 (&xc)[MT]) {
     uint32_t wa[UW], wb[UW];
-    lds_codes<UW>(smem, q.ca, colstride, q.sa, word0, wa);
-    lds_codes<UW>(smem, q.cb, colstride, q.sb, word0, wb);
-    const uint16_t sah = lds16(ka), sbh = lds16(kb8);
+    lds_codes<UW>(smem, ca, colstride, swa, word0, wa);
+    lds_codes<UW>(smem, cb8, colstride, swb, word0, wb);
+    const int kofs = (grp >> 3) * kblk + (grp & 7) * 2;
+    const uint16_t sah = lds16(smem + ka + kofs), sbh = lds16(smem + kb8 + kofs);
     uint16_t eah = 0, ebh = 0;
-    if (FMT == 4 && wi0 == 0) {
-      eah = lds16(ka + coef_bytes);
-      ebh = lds16(kb8 + coef_bytes);
+    if (FMT == 4 && first) {
+      eah = lds16(smem + ka + coef_bytes + kofs);
+      ebh = lds16(smem + kb8 + coef_bytes + kofs);
     }
-    float4 xc[MT];
-#pragma unroll
-    for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tok[cb] * NG + grp];
-    float d[NA][MT][4];
-#pragma unroll
-    for (int a = 0; a < NA; a++)
-#pragma unroll
-      for (int cb = 0; cb < MT; cb++) d[a][cb][0] = d[a][cb][1] = d[a][cb][2] = d[a][cb][3] = 0.0f;
+    float d[2][MT][4];
 #pragma unroll
     for (int u = 0; u < UW; u++) {
-      const int pos = pst + u;
       if constexpr (FMT == 4) {
         const uint32_t w = wa[u], v = wb[u], w8 = w >> 8, v8 = v >> 8;
 #pragma unroll
         for (int cb = 0; cb < MT; cb++) {
-          const uint4 b = lds128(smem + (baddr[cb] + pos * bstride[cb]));
-          mma_f16(d[(2 * u) % NA][cb], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
-          mma_f16(d[(2 * u + 1) % NA][cb], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u,
-                  b.z, b.w);
+          const uint4 b = bf[cb][u];
+          if (u == 0) {
+            mma_f16_z(d[0][cb], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
+            mma_f16_z(d[1][cb], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
+          } else {
+            mma_f16(d[0][cb], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
+            mma_f16(d[1][cb], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
+          }
         }
       } else if constexpr (FMT == 8) {
         if ((u & 1) == 0) {
@@ -560,11 +571,18 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           const uint32_t w1 = wa[u + 1] ^ 0x80808080u, v1 = wb[u + 1] ^ 0x80808080u;
 #pragma unroll
           for (int cb = 0; cb < MT; cb++) {
-            const uint4 b = lds128(smem + (baddr[cb] + (pos >> 1) * bstride[cb]));
-            mma_f16(d[u % NA][cb], prmt(w0, 0u, 0x4140u), prmt(v0, 0u, 0x4140u), prmt(w0, 0u, 0x4342u),
-                    prmt(v0, 0u, 0x4342u), b.x, b.y);
-            mma_f16(d[(u + 1) % NA][cb], prmt(w1, 0u, 0x4140u), prmt(v1, 0u, 0x4140u), prmt(w1, 0u, 0x4342u),
-                    prmt(v1, 0u, 0x4342u), b.z, b.w);
+            const uint4 b = bf[cb][u >> 1];
+            if (u == 0) {
+              mma_f16_z(d[0][cb], prmt(w0, 0u, 0x4140u), prmt(v0, 0u, 0x4140u), prmt(w0, 0u, 0x4342u),
+                        prmt(v0, 0u, 0x4342u), b.x, b.y);
+              mma_f16_z(d[1][cb], prmt(w1, 0u, 0x4140u), prmt(v1, 0u, 0x4140u), prmt(w1, 0u, 0x4342u),
+                        prmt(v1, 0u, 0x4342u), b.z, b.w);
+            } else {
+              mma_f16(d[0][cb], prmt(w0, 0u, 0x4140u), prmt(v0, 0u, 0x4140u), prmt(w0, 0u, 0x4342u),
+                      prmt(v0, 0u, 0x4342u), b.x, b.y);
+              mma_f16(d[1][cb], prmt(w1, 0u, 0x4140u), prmt(v1, 0u, 0x4140u), prmt(w1, 0u, 0x4342u),
+                      prmt(v1, 0u, 0x4342u), b.z, b.w);
+            }
           }
         }
       } else {
@@ -581,9 +599,14 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           }
 #pragma unroll
           for (int cb = 0; cb < MT; cb++) {
-            const uint4 b = lds128(smem + (baddr[cb] + (pos * 4 + jp) * bstride[cb]));
-            mma_f16(d[(8 * u + 2 * jp) % NA][cb], aw[0], av[0], aw[1], av[1], b.x, b.y);
-            mma_f16(d[(8 * u + 2 * jp + 1) % NA][cb], aw[2], av[2], aw[3], av[3], b.z, b.w);
+            const uint4 b = bf[cb][4 * u + jp];
+            if (u == 0 && jp == 0) {
+              mma_f16_z(d[0][cb], aw[0], av[0], aw[1], av[1], b.x, b.y);
+              mma_f16_z(d[1][cb], aw[2], av[2], aw[3], av[3], b.z, b.w);
+            } else {
+              mma_f16(d[0][cb], aw[0], av[0], aw[1], av[1], b.x, b.y);
+              mma_f16(d[1][cb], aw[2], av[2], aw[3], av[3], b.z, b.w);
+            }
           }
         }
       }
@@ -592,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     // x-only correction e X once per group
     float sa = h2f(sah), sbv = h2f(sbh);
     float ea = 0.0f, eb = 0.0f;
-    if (wi0 == 0) {
+    if (first) {
       if constexpr (FMT == 4) {
         ea = h2f(eah);
         eb = h2f(ebh);
@@ -610,30 +633,52 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     }
 #pragma unroll
     for (int cb = 0; cb < MT; cb++) {
-      float d0 = d[0][cb][0] + d[0][cb][1], d1 = d[0][cb][2] + d[0][cb][3];
-#pragma unroll
-      for (int a = 1; a < NA; a++) {
-        d0 += d[a][cb][0] + d[a][cb][1];
-        d1 += d[a][cb][2] + d[a][cb][3];
-      }
+      const float d0 = (d[0][cb][0] + d[0][cb][1]) + (d[1][cb][0] + d[1][cb][1]);
+      const float d1 = (d[0][cb][2] + d[0][cb][3]) + (d[1][cb][2] + d[1][cb][3]);
       const float ta = fmaf(sa, d0, ea * xc[cb].x), tb = fmaf(sbv, d1, eb * xc[cb].x);
       acc[cb][0] = fmaf(ta * xc[cb].y, xc[cb].z, acc[cb][0]);
       acc[cb][1] = fmaf(tb * xc[cb].y, xc[cb].z, acc[cb][1]);
     }
   };
 
+  uint4 bf[MT][NQ];
+  float4 xc[MT];
   if (!wide) {
     if (ok && se > sb) {
-      int tile = sb / spt, pst = (sb - tile * spt) * UW;
-      Rows q = rows_at(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
+      int tile = sb / spt;
+      int pst = (sb - tile * spt) * UW;                        // lane word position in the tile row
+      int pst0 = pst;                                          // position of the run's first step in this tile
+      int wi = pst & (wl - 1);
+      int grp = ((pst >> lg_wl) << LG_GPM) + gsel_lane;
+      int word0 = grp * wpg + wofs_lane + wi;
+      set_rows(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
       for (int s = sb; s < se; s++) {
-        step(q, pst);
+        load_b(pst, bf);
+#pragma unroll
+        for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tokofs[cb] + grp];
+        step(word0, grp, wi == 0, bf, xc);
         pst += UW;
+        wi += UW;
+        word0 += UW;
+        if (wi == wl) {
+          wi = 0;
+          grp += GPM;
+          word0 += GPM * wpg - wl;
+        }
         if (pst == npos || s + 1 == se) {
           flush(cw + tile);                           // (warp, tile) -> warp + tile is one-to-one
-          pst = 0;
+          // the warps that took the tile's first and last k-step record
+          // themselves for the final sums
+          if (lane == 0 && pst0 == 0) tw[2 * tile] = cw;
+          if (lane == 0 && pst == npos) tw[2 * tile + 1] = cw;
+          if (s + 1 == se) break;
           tile++;
-          q = rows_at(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
+          pst = 0;
+          pst0 = 0;
+          wi = 0;
+          grp = gsel_lane;
+          word0 = grp * wpg + wofs_lane;
+          set_rows(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
         }
       }
     }
@@ -643,8 +688,25 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       const int tile = u >> lg_nks, ks = u & (nks - 1);
       const int slot = tile % S;
       if (!__all_sync(0xffffffffu, wait_bounded(bars + 8 * slot, (tile / S) & 1, ctl))) { ok = false; break; }
-      const Rows q = rows_at(slot * stage_bytes, g, g + 8);
-      for (int s = ks * spu; s < (ks + 1) * spu; s++) step(q, s * UW);
+      set_rows(slot * stage_bytes, g, g + 8);
+      int pst = ks * spu * UW;
+      int wi = pst & (wl - 1);
+      int grp = ((pst >> lg_wl) << LG_GPM) + gsel_lane;
+      int word0 = grp * wpg + wofs_lane + wi;
+      for (int s = 0; s < spu; s++) {
+        load_b(pst, bf);
+#pragma unroll
+        for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tokofs[cb] + grp];
+        step(word0, grp, wi == 0, bf, xc);
+        pst += UW;
+        wi += UW;
+        word0 += UW;
+        if (wi == wl) {
+          wi = 0;
+          grp += GPM;
+          word0 += GPM * wpg - wl;
+        }
+      }
       flush(u);
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8 * (S + slot));
@@ -659,11 +721,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     const int tile = r >> 4, rr = r & (kTileRows - 1);
     float sum = 0.0f;
     if (!wide) {
-      const int w1 = last_warp(tile, spt, W, total_steps);
-      for (int w = first_warp(tile, spt, W, total_steps); w <= w1; w++)
-        sum += red[((size_t)(w + tile) * M + m) * kTileRows + rr];
+      const int w1 = tw[2 * tile + 1];
+      for (int w = tw[2 * tile]; w <= w1; w++) sum += red[((w + tile) * M + m) * kTileRows + rr];
     } else {
-      for (int ks = 0; ks < nks; ks++) sum += red[((size_t)(tile * nks + ks) * M + m) * kTileRows + rr];
+      for (int ks = 0; ks < nks; ks++) sum += red[((tile * nks + ks) * M + m) * kTileRows + rr];
     }
     return sum;
   };
@@ -682,11 +743,14 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   if (!fin) return;
   float *__restrict__ y = p.y;
   const int N = p.N;
-  for (int idx = ct; idx < rows * M; idx += nthreads) {
-    const int m = idx / rows, r = idx - m * rows;
-    y[(int64_t)m * N + n_begin + r] = total(r, m);
+  if (M == 1) {
+    for (int r = ct; r < rows; r += nthreads) y[n_begin + r] = total(r, 0);
+  } else {
+    for (int idx = ct; idx < rows * M; idx += nthreads) {
+      const int m = idx / rows, r = idx - m * rows;
+      y[(int64_t)m * N + n_begin + r] = total(r, m);
+    }
   }
-  (void)K;
 }
 
 // ---------------------------------------------------------------- host plan
@@ -715,13 +779,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode() {
   return fn;
 }
 
-// Instantiated (format, UW, MT) combinations; the greedy-argmax variants
-// mirror the plain ones (a fused argmax must sum exactly as the plain product).
-bool have_variant(int fmt, int uw, int mt) {
-  if (fmt == 4) return mt == 1 ? (uw == 2 || uw == 4 || uw == 8) : (uw == 2 || uw == 4);
-  if (fmt == 8) return uw == 4 || uw == 8;
-  return fmt == 1 && mt == 1 && uw == 2;
-}
+bool have_variant(int fmt, int uw, int mt, int gpm, bool argmax);
 
 int ilog2(int v) {
   int l = 0;
@@ -771,7 +829,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   int pstr0 = nact0 * 16 + 16, pstr1 = nact1 ? nact1 * 16 + 16 : 0;
   size_t bbytes = (size_t)nj2 * (pstr0 + pstr1);
   const size_t xsbytes = (size_t)M * NG * 16;              // {2^-24 sum x', f1, f2} per (token, group)
-  const size_t misc = 16 + kAmScratch + 16 + 1024;        // zero block, argmax scratch, abort, alignment
+  const size_t misc = 16 + 256 + kAmScratch + 16 + 1024;  // zero block, tile table, argmax scratch, abort, alignment
 
   // rows per CTA: the 8-row blocks of N split evenly over one CTA per SM (so
   // that no SM holds two CTAs of one product); a slab is copied as 8-row
@@ -785,7 +843,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   int best_uw = 0, best_wide = 0, best_S = 1, best_nks = 1, best_spt = 0;
   double best_cost = 1e30;
   for (int uw = 8; uw >= 2; uw >>= 1) {
-    if (wl % uw != 0 || !have_variant(fmt, uw, mt)) continue;
+    if (wl % uw != 0 || !have_variant(fmt, uw, mt, gpm, argmax)) continue;
     const int spt = npos / uw;
     const double step_cost = uw * (1.0 + 0.15 * 8 / (uw * MPW));   // relative cost of one k-step
     // resident slab (up to 256 rows): warps take runs of k-steps
@@ -875,6 +933,8 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   off += (best_wide ? (size_t)nt_red * best_nks : (size_t)(15 + ntiles)) * M * kTileRows * 4;
   p.off_zero = (int)off;
   off += 16;
+  p.off_tw = (int)off;
+  off += 8 * 32;
   p.off_bar = (int)off;
   off += 8 * 2 * p.stages + 16;
   off = (off + 15) & ~(size_t)15;
@@ -918,10 +978,10 @@ bool encode_maps(const TcParams &p, const void *codes, const void *scales, const
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int UW, int MT, bool ARGMAX>
+template <int FMT, int UW, int MT, int GPM, bool ARGMAX>
 cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUtensorMap &tb, const TcParams &p,
                          int grid, size_t smem, cudaStream_t s) {
-  auto kern = gemv_tc_kernel<FMT, UW, MT, ARGMAX>;
+  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, ARGMAX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -939,30 +999,35 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
   return cudaLaunchKernelEx(&cfg, kern, tc, ts, tb, p);
 }
 
+// The instantiated kernels: (format, k-step UW, column blocks MT, groups per
+// MMA GPM); the greedy-argmax variants mirror the one-token ones, so that a
+// fused argmax sums exactly as the plain product.
 template <bool ARGMAX>
-cudaError_t launch_tc(int fmt, int uw, int mt, const CUtensorMap &tc, const CUtensorMap &ts, const CUtensorMap &tb,
-                      const TcParams &p, int grid, size_t smem, cudaStream_t s) {
-  if (fmt == 4) {
-    if (mt == 1) {
-      if (uw == 8) return launch_tc_as<4, 8, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
-      if (uw == 4) return launch_tc_as<4, 4, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
-      if (uw == 2) return launch_tc_as<4, 2, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
-    } else if constexpr (!ARGMAX) {
-      if (uw == 4) return launch_tc_as<4, 4, 2, false>(tc, ts, tb, p, grid, smem, s);
-      if (uw == 2) return launch_tc_as<4, 2, 2, false>(tc, ts, tb, p, grid, smem, s);
-    }
-  } else if (fmt == 8) {
-    if (mt == 1) {
-      if (uw == 8) return launch_tc_as<8, 8, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
-      if (uw == 4) return launch_tc_as<8, 4, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
-    } else if constexpr (!ARGMAX) {
-      if (uw == 8) return launch_tc_as<8, 8, 2, false>(tc, ts, tb, p, grid, smem, s);
-      if (uw == 4) return launch_tc_as<8, 4, 2, false>(tc, ts, tb, p, grid, smem, s);
-    }
-  } else if (fmt == 1 && mt == 1 && uw == 2) {
-    return launch_tc_as<1, 2, 1, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+cudaError_t launch_tc(int fmt, int uw, int mt, int gpm, const CUtensorMap &tc, const CUtensorMap &ts,
+                      const CUtensorMap &tb, const TcParams &p, int grid, size_t smem, cudaStream_t s) {
+#define QMM_TC(F_, U_, T_, G_)                                                        \
+  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_)                                 \
+    return launch_tc_as<F_, U_, T_, G_, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+  QMM_TC(4, 4, 1, 4) QMM_TC(4, 2, 1, 4)
+  QMM_TC(8, 8, 1, 4) QMM_TC(8, 4, 1, 4)
+  QMM_TC(1, 2, 1, 4)
+  if constexpr (!ARGMAX) {
+    QMM_TC(4, 4, 1, 2) QMM_TC(4, 2, 1, 2)
+    QMM_TC(8, 8, 1, 2) QMM_TC(8, 4, 1, 2)
+    QMM_TC(4, 4, 1, 1) QMM_TC(4, 2, 1, 1) QMM_TC(4, 4, 2, 1) QMM_TC(4, 2, 2, 1)
+    QMM_TC(8, 8, 1, 1) QMM_TC(8, 4, 1, 1) QMM_TC(8, 8, 2, 1) QMM_TC(8, 4, 2, 1)
   }
+#undef QMM_TC
   return cudaErrorNotSupported;
+}
+
+bool have_variant(int fmt, int uw, int mt, int gpm, bool argmax) {
+  if (gpm == 4) return mt == 1 && ((fmt == 4 && (uw == 4 || uw == 2)) || (fmt == 8 && (uw == 8 || uw == 4)) ||
+                                   (fmt == 1 && uw == 2));
+  if (argmax) return false;
+  if (fmt == 4) return (uw == 4 || uw == 2) && (gpm == 1 || mt == 1);
+  if (fmt == 8) return (uw == 8 || uw == 4) && (gpm == 1 || mt == 1);
+  return false;
 }
 
 }  // namespace
@@ -978,7 +1043,7 @@ cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t
   if (!encode_maps(p, codes, scales, biases, tc, ts, tb)) return cudaErrorNotSupported;
   p.x = x;
   p.y = y;
-  return launch_tc<false>(bits, uw, M > 4 ? 2 : 1, tc, ts, tb, p, grid, smem, s);
+  return launch_tc<false>(bits, uw, M > 4 ? 2 : 1, p.gpm, tc, ts, tb, p, grid, smem, s);
 }
 
 cudaError_t launch_gemv_tc_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
@@ -993,7 +1058,7 @@ cudaError_t launch_gemv_tc_argmax(const float *x, const uint32_t *codes, const u
   p.x = x;
   p.y = nullptr;
   p.am = w;
-  return launch_tc<true>(bits, uw, 1, tc, ts, tb, p, grid, smem, s);
+  return launch_tc<true>(bits, uw, 1, p.gpm, tc, ts, tb, p, grid, smem, s);
 }
 
 cudaError_t read_clear_tc_status(int *status, cudaStream_t s) {

@@ -78,9 +78,7 @@ extern "C" int qmm_gemv_argmax_noalloc(const float *x, const uint32_t *codes, co
   uint8_t *ws = static_cast<uint8_t *>(scratch);
   qmm::ArgmaxWork w{reinterpret_cast<unsigned *>(ws), reinterpret_cast<float *>(ws + 16),
                     reinterpret_cast<int32_t *>(ws + 16 + 4 * qmm::kArgmaxMaxCtas), idx, val};
-  cudaError_t e = qmm::launch_gemv_tc_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
-  if (e == cudaErrorNotSupported)
-    e = qmm::launch_gemv_stream_argmax(x, codes, scales, biases, N, K, bits, group, w, stream);
+  const cudaError_t e = qmm::launch_gemv_argmax_fused(x, codes, scales, biases, N, K, bits, group, w, stream);
   if (e == cudaErrorNotSupported) return QMM_ERR_UNSUPPORTED;
   return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }

@@ -51,6 +51,12 @@ cudaError_t launch_gemv_stream(const float *x, const uint32_t *codes, const uint
 cudaError_t launch_gemv_stream_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
                                       const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
                                       const ArgmaxWork &w, cudaStream_t s);
+// The fused M == 1 greedy head: the tensor-core kernel for INT4 (as
+// launch_gemv), the streamed kernel first for INT8 and Q1, then the
+// tensor-core kernel.  cudaErrorNotSupported if none takes the shape.
+cudaError_t launch_gemv_argmax_fused(const float *x, const uint32_t *codes, const uint16_t *scales,
+                                     const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
+                                     const ArgmaxWork &w, cudaStream_t s);
 // Per row m < M of logits [M, N]: idx[m] = argmax (NaN first, ties to the lower index), val[m] its value.
 cudaError_t launch_argmax_rows(const float *logits, int M, int64_t N, int32_t *idx, float *val, cudaStream_t s);
 
