@@ -43,8 +43,8 @@ HEADLINE_DOWN = "decode_int4_down_k6144_n2048"
 WORKLOAD_NAME = "decode_int4_g64_mlp_up_k2048_n6144+down_k6144_n2048"
 METRIC = "decode qGEMV weight-GB/s (% of HBM peak)"
 NOMINAL_HBM_GBS = 8000.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemv_stream_int4_decode_mlp.md")
-GEMV_SOURCE = os.path.join(ROOT, "quantized_weight_gb300", "csrc", "gemv_stream.cu")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+HEADLINE_KERNEL = "gemv_tc_kernel (INT4 tensor-core decode product)"
 
 
 # ---------------------------------------------------------------- algorithmic work
@@ -240,6 +240,7 @@ def measure_config(name, torch, qmm, stream, pk, reps=20):
         gbs = gemv_bytes(w.M, w.N, w.K, w.bits, w.group) / sec / 1e9
         out.update({"gbs": gbs, "frac_of_measured_hbm": gbs / pk["hbm_gbs"],
                     "frac_of_8tbs": gbs / NOMINAL_HBM_GBS})
+    out["parity_vs_oracle"] = sampled_parity(w, d, ys[0].cpu().numpy())
     del ts, ys, chain
     torch.cuda.empty_cache()
     return out
@@ -270,8 +271,14 @@ def measure_extra(name, torch, qmm, stream, pk, reps=20):
         copies = max(2, -(-4 * L2 // nbytes))
         ts = replicate(t, copies, torch)
         ws = [qmm.argmax_workspace(1, N) for _ in range(copies)]
-        calls = [(lambda i=i: qmm.gemv_argmax(ts[i]["x"], ts[i]["packed"], ts[i]["scales"], ts[i]["biases"], N, 4,
-                                              64, ws[i])) for i in range(copies)]
+        res = [None] * copies
+
+        def head(i):
+            res[i] = qmm.gemv_argmax(ts[i]["x"], ts[i]["packed"], ts[i]["scales"], ts[i]["biases"], N, 4, 64,
+                                     ws[i], idx=res[i][0] if res[i] else None, val=res[i][1] if res[i] else None)
+        calls = [(lambda i=i: head(i)) for i in range(copies)]
+        for i in range(copies):
+            head(i)                              # result tensors exist before capture
     elif kind == "quantize":
         w = torch.randn((N, K), device="cuda", generator=torch.Generator("cuda").manual_seed(0)) * 0.05
         nbytes = N * K * 4 + N * K // 2 + N * (K // 64) * 4
@@ -295,26 +302,102 @@ def measure_extra(name, torch, qmm, stream, pk, reps=20):
     chain = Chain(calls, torch).capture(stream)
     sec = time_graph(chain, reps, 3, torch, stream) / copies
     gbs = nbytes / sec / 1e9
+    torch.cuda.synchronize()
+    if kind == "argmax":
+        parity = head_parity(d, N, K, int(res[0][0].item()), float(res[0][1].item()))
+    elif kind == "quantize":
+        parity = quantize_parity(ws[0].cpu().numpy(), [o.cpu().numpy() for o in outs[0]])
+    else:
+        parity = gather_parity(d, ids.cpu().numpy(), outs[0].cpu().numpy(), K)
     del chain
     torch.cuda.empty_cache()
     return {"kind": kind, "M": M, "N": N, "K": K, "us_per_launch": sec * 1e6, "bytes_per_launch": nbytes,
-            "gbs": gbs, "frac_of_measured_hbm": gbs / pk["hbm_gbs"], "copies": copies}
+            "gbs": gbs, "frac_of_measured_hbm": gbs / pk["hbm_gbs"], "copies": copies,
+            "parity_vs_oracle": parity}
+
+
+def head_parity(d, N, K, idx, val):
+    """The greedy head's winner against the oracle's full FP64 logits: the
+    winner's logit must be within the float32 accumulation bound of the
+    largest one, and its reported value within that bound of its own logit."""
+    import oracle
+    y = oracle.qmm_f32x(d["x"], oracle.pack(d["codes"], 4), d["scales"], d["biases"], N, K, 4, 64)[0]
+    top = int(np.argmax(y))
+    # |sum of K float32 products| error bound: K * 2^-23 * sum |x_k w_k| (taken loosely over the winner row)
+    w = oracle.dequant(oracle.pack(d["codes"][[idx]], 4), d["scales"][[idx]], d["biases"][[idx]], 1, K, 4, 64)[0]
+    bound = K * 2.0 ** -23 * float(np.sum(np.abs(d["x"][0].astype(np.float64) * w)))
+    return {"oracle_argmax": top, "idx": idx, "gap_to_max": float(y[top] - y[idx]),
+            "val_err": float(abs(val - y[idx])), "bound": bound,
+            "ok": bool(y[top] - y[idx] <= 2 * bound and abs(val - y[idx]) <= bound)}
+
+
+def quantize_parity(w, outs, rows=64):
+    """Bit-exact comparison of sampled rows of the stored-format quantizer's
+    outputs (packed codes, scales, biases) with the oracle's quantizer."""
+    import oracle
+    sel = np.random.default_rng(1).choice(w.shape[0], rows, replace=False)
+    codes, sc, bi = oracle.quantize_affine4_f32(w[sel], 64)
+    packed = oracle.pack(codes, 4)
+    same = (np.array_equal(outs[0][sel].view(np.uint32), packed.view(np.uint32))
+            and np.array_equal(outs[1][sel].view(np.uint16), sc) and np.array_equal(outs[2][sel].view(np.uint16), bi))
+    return {"rows": rows, "bit_exact": bool(same)}
+
+
+def gather_parity(d, ids, out, K, rows=32):
+    """Sampled gathered rows against the oracle's dequantized table rows (bit-exact)."""
+    import oracle
+    pos = np.random.default_rng(1).choice(len(ids), rows, replace=False)
+    sel = ids[pos]
+    ref = oracle.dequant(oracle.pack(d["codes"][sel], 4), d["scales"][sel], d["biases"][sel], rows, K, 4, 64)
+    same = np.array_equal(out[pos].astype(np.float32).view(np.uint32), ref.astype(np.float32).view(np.uint32))
+    return {"rows": rows, "bit_exact": bool(same)}
+
+
+def sources_sha256(paths):
+    """sha256 over the listed repository files, in order."""
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def traffic_from_profile():
-    """dram bytes per launch of the headline kernel from the committed ncu summary,
-    or None if the summary is missing or the kernel source changed since."""
-    if not os.path.exists(PROFILE_SUMMARY):
+    """DRAM bytes per launch of the headline kernel, from the committed ncu
+    figures in profiles/traffic.json, or None if the file is missing or a
+    source file the kernel is built from changed since the capture."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
-    text = open(PROFILE_SUMMARY).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    h = re.search(r"gemv_source_sha256:\s*([0-9a-f]{16,64})", text)
-    if not m or not h:
+    try:
+        d = json.load(open(TRAFFIC_JSON))
+        rec = d["headline"]
+        if sources_sha256(rec["sources"]) != rec["sources_sha256"]:
+            return None
+        return float(rec["bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    cur = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
-    if not cur.startswith(h.group(1)):
-        return None
-    return float(m.group(1))
+
+
+# ---------------------------------------------------------------- sampled parity
+
+def sampled_parity(w, d, y, nsample=256, seed=1):
+    """Relative L2 error and the largest element error (over the oracle's
+    largest |y|) of `nsample` outputs of y (a host float32 array [M, N])
+    against the oracle evaluated at those outputs only."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    ms = rng.integers(0, w.M, nsample)
+    ns = rng.integers(0, w.N, nsample)
+    x = d["x_bf16"] if w.prefill else d["x"]
+    sel = np.unique(ns)
+    remap = {int(n): i for i, n in enumerate(sel)}
+    sub = oracle.pack(d["codes"][sel], w.bits)
+    ref = oracle.qmm_sampled(x, sub, d["scales"][sel], None if d["biases"] is None else d["biases"][sel],
+                             ms, np.array([remap[int(n)] for n in ns]), len(sel), w.K, w.bits, w.group)
+    got = y[ms, ns].astype(np.float64)
+    err = got - ref
+    return {"samples": int(nsample), "rel_l2": float(np.linalg.norm(err) / np.linalg.norm(ref)),
+            "max_err_over_max_ref": float(np.max(np.abs(err)) / np.max(np.abs(ref)))}
 
 
 # ---------------------------------------------------------------- multi-rank host logic
@@ -493,6 +576,7 @@ def main():
     ref = oracle.qmm_sampled(up_d["x"], oracle.pack(up_d["codes"], 4), up_d["scales"], up_d["biases"],
                              np.zeros_like(ns), ns, up_w.N, up_w.K, 4, 64)
     parity = float(np.linalg.norm(y0[ns] - ref) / np.linalg.norm(ref))
+    parity_dn = sampled_parity(dn_w, dn_d, y_dn[0].cpu().numpy())
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -570,6 +654,43 @@ def main():
     e2e_sec = slowest_rank_seconds(f0.elapsed_time(f1) / 1000.0, world, "cuda")
     e2e_val = job_gbs(step_bytes, e2e_steps, world, e2e_sec)
 
+    # the same end-to-end step without a graph: every product is its own C-ABI
+    # call (qmm_gemv through ctypes, arguments marshalled in advance), so the
+    # library's host-side validation and launch run inside the timed region
+    L = qmm.lib()
+    sh = stream.cuda_stream
+    abi_args = []
+    for i in range(layers):
+        for t, w, X, Y in ((ups[i], up_w, X_up, Y_up), (dns[i], dn_w, X_dn, Y_dn)):
+            abi_args.append((X[i:i + 1].data_ptr(), t["packed"].data_ptr(), t["scales"].data_ptr(),
+                             t["biases"].data_ptr(), Y[i:i + 1].data_ptr(), 1, w.N, w.K, 4, 64, sh))
+
+    def percall_step():
+        X_up.copy_(X_up_h, non_blocking=True)
+        X_dn.copy_(X_dn_h, non_blocking=True)
+        for a in abi_args:
+            rc = L.qmm_gemv(*a)
+            if rc != 0:
+                raise RuntimeError(f"qmm_gemv returned {rc}")
+        Y_up_h.copy_(Y_up, non_blocking=True)
+        Y_dn_h.copy_(Y_dn, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            percall_step()
+        stream.synchronize()
+        barrier()
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            percall_step()
+        f1.record(stream)
+        f1.synchronize()
+        barrier()
+    pc_ok = bool(torch.equal(Y_up_h[0].cuda(), qmm.gemv(X_up[0:1], ups[0]["packed"], ups[0]["scales"],
+                                                        ups[0]["biases"], up_w.N, 4, 64)[0]))
+    pc_sec = slowest_rank_seconds(f0.elapsed_time(f1) / 1000.0, world, "cuda")
+    pc_val = job_gbs(step_bytes, e2e_steps, world, pc_sec)
+
     del chain, e2e_chain
     torch.cuda.empty_cache()
 
@@ -597,23 +718,30 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "graph": "CUDA graph per step, programmatic dependent launch between products"},
         "frac_of_8tbs": value / world / NOMINAL_HBM_GBS,
-        "parity": {"sampled_rel_l2_vs_oracle": parity, "tolerance": 1e-5},
+        "parity": {"sampled_rel_l2_vs_oracle": parity, "down_projection": parity_dn, "tolerance": 1e-5},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic_from_profile(),
-                     "kernel": "gemv_stream_kernel<4> (INT4 decode product)",
+                     "kernel": HEADLINE_KERNEL,
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "results_checked": e2e_ok,
                 "path": "pinned host x -> device (one copy per projection), the 2L qmm.gemv calls replayed "
-                        "from a CUDA graph, device y -> pinned host (one copy per projection)"},
+                        "from a CUDA graph, device y -> pinned host (one copy per projection)",
+                "per_call": {"value": pc_val, "unit": "GB/s", "ms_per_step": pc_sec / e2e_steps * 1e3,
+                             "results_checked": pc_ok,
+                             "path": "the same copies, and the 2L products as 2L qmm_gemv C-ABI calls from "
+                                     "the host each step (no graph)"}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "per_config": per_config,
     }
     if rank == 0 and world == 1:
         nbytes, el, th, nl = oracle_sample(args.oracle_seconds)
+        n1, el1, _, nl1 = oracle_sample(args.oracle_seconds, nthreads=1)
         line["cpu_baseline"] = {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": th, "kind": "oracle",
-                                "sample": f"{nl} layers (up + down) of {WORKLOAD_NAME}, {el:.1f} s"}
+                                "sample": f"{nl} layers (up + down) of {WORKLOAD_NAME}, {el:.1f} s",
+                                "single_thread": {"value": n1 / el1 / 1e9, "unit": "GB/s", "cores": 1,
+                                                  "sample": f"{nl1} layers (up + down), {el1:.1f} s"}}
     elif rank == 0:
         line["cpu_baseline"] = None
     if rank == 0:

@@ -33,7 +33,9 @@
  * pointer past the call, and never allocates or frees device memory in any
  * call (the residency rule of the "15 year old GPU" page, section "Cost 2:
  * memory is allocated and freed on every layer").  Device pointers must be
- * 16-byte aligned.
+ * 16-byte aligned, except the idx and val outputs of the argmax heads, which
+ * need only their element's 4-byte alignment (so a decode loop can write the
+ * token straight into tokens[t]).
  *
  * Asynchrony.  Every call validates its arguments on the host and then only
  * enqueues kernels on `stream` (a cudaStream_t; NULL is the legacy default
@@ -63,7 +65,7 @@ typedef enum {
     QMM_OK = 0,
     QMM_ERR_ARG = -1,             /* NULL pointer, or a biases pointer that contradicts bits */
     QMM_ERR_SHAPE = -2,           /* negative size, K % 32, K % group, M outside the entry's range */
-    QMM_ERR_ALIGN = -3,           /* a device pointer not 16-byte aligned */
+    QMM_ERR_ALIGN = -3,           /* a device pointer not 16-byte aligned (idx, val: 4-byte) */
     QMM_ERR_UNSUPPORTED = -4,     /* bits / group combination this entry does not implement */
     QMM_ERR_CUDA = -5,            /* a CUDA runtime call or launch failed */
     QMM_ERR_DEVICE_TIMEOUT = -6   /* a bounded device-side wait ran out (see qmm_check) */
@@ -151,7 +153,8 @@ int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scal
  *   bytes, 16-byte aligned, owned by the caller, whose first 16 bytes are zero
  *   before the first call (for instance from cudaMemset); every call leaves
  *   them zero again.  Two calls in flight at the same time must not share a
- *   workspace.  idx: int32 [M]; val: float32 [M] or NULL.
+ *   workspace.  idx: int32 [M]; val: float32 [M] or NULL (both 4-byte
+ *   aligned; QMM_ERR_ALIGN otherwise).
  */
 size_t qmm_gemv_argmax_workspace_size(int64_t M, int64_t N);
 int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
@@ -169,8 +172,11 @@ int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scale
  *   the allocator between tokens, or a C host without an allocator).
  *   Rules: the array's counter is zero when the library loads and every call
  *   leaves it zero; the first call on each device looks the array's address
- *   up (cudaGetSymbolAddress) and caches it, so make that first call before
- *   any stream capture begins; all calls on a device share the array, so no
+ *   up (cudaGetSymbolAddress) and caches it with the current context, so make
+ *   the first call in each context before any stream capture begins; a call
+ *   in another context than the cached one (after cudaDeviceReset, or after
+ *   the primary context was released and created again) looks the address up
+ *   anew; all calls on a device share the array, so no
  *   two calls may be in flight at once (calls in order on one stream are
  *   fine).  Shapes that the fused M == 1 kernel does not take, or that would
  *   need more than 1024 CTAs, return QMM_ERR_UNSUPPORTED.  Other argument

@@ -13,6 +13,7 @@
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool bits_ok(int bits) { return bits == 1 || bits == 4 || bits == 8; }
 bool group_ok(int group) { return group == 32 || group == 64 || group == 128; }
 constexpr int64_t kMaxDim = (int64_t)1 << 31;   // N, K, M each fit in int for the kernels
@@ -43,7 +44,7 @@ const char *qmm_status_string(int status) {
     case QMM_OK: return "QMM_OK";
     case QMM_ERR_ARG: return "QMM_ERR_ARG: null pointer or biases pointer inconsistent with bits";
     case QMM_ERR_SHAPE: return "QMM_ERR_SHAPE: size out of range or not a multiple of 32 / group";
-    case QMM_ERR_ALIGN: return "QMM_ERR_ALIGN: device pointer not 16-byte aligned";
+    case QMM_ERR_ALIGN: return "QMM_ERR_ALIGN: device pointer not aligned (16 bytes; idx and val: 4 bytes)";
     case QMM_ERR_UNSUPPORTED: return "QMM_ERR_UNSUPPORTED: bits/group combination not implemented";
     case QMM_ERR_CUDA: return "QMM_ERR_CUDA: a CUDA call or kernel launch failed";
     case QMM_ERR_DEVICE_TIMEOUT: return "QMM_ERR_DEVICE_TIMEOUT: a bounded device-side wait ran out";
@@ -129,7 +130,8 @@ int qmm_gemv_argmax(const float *x, const uint32_t *codes, const uint16_t *scale
   if (!x || !codes || !idx || !workspace) return QMM_ERR_ARG;
   int st = check_coeffs(scales, biases, bits);
   if (st != QMM_OK) return st;
-  if (!aligned16(x) || !aligned16(codes) || !aligned16(workspace) || !aligned16(idx)) return QMM_ERR_ALIGN;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(workspace) || !aligned4(idx) || (val && !aligned4(val)))
+    return QMM_ERR_ALIGN;
   if (workspace_bytes < qmm_gemv_argmax_workspace_size(M, N)) return QMM_ERR_SHAPE;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (M == 1) {

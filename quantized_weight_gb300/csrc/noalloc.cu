@@ -16,9 +16,11 @@
 //     since that would need room for the logits);
 //   * the counter must be zero when a call starts: the array is zero when the
 //     module loads, and every call's last CTA sets it back to zero;
-//   * the address of the array is looked up once per device with
-//     cudaGetSymbolAddress and cached; make the first call on each device
-//     before any stream capture begins;
+//   * the address of the array is looked up with cudaGetSymbolAddress and
+//     cached per device together with the context that was current at the
+//     lookup; a call made in another context (after cudaDeviceReset, or once
+//     the primary context was destroyed and created again) looks it up anew.
+//     Make the first call in each context before any stream capture begins;
 //   * all calls on a device share the array, so two calls must never be in
 //     flight at the same time (for instance on two streams): they would race
 //     on the counter and the winners.  Calls issued one after another on one
@@ -26,6 +28,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "qmm.h"
@@ -40,23 +43,50 @@ static __device__ __align__(256) unsigned char g_argmax_scratch[kScratchBytes];
 
 std::mutex g_scratch_mutex;
 void *g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// The device address of g_argmax_scratch on the current device (cached).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link to libcuda).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+  });
+  return fn;
+}
+
+// The device address of g_argmax_scratch in the current context.  The cached
+// address is reused only while the context it was looked up in is current.
 cudaError_t scratch_address(void **addr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (!ctx || ctx != g_scratch_ctx[dev] || !g_scratch_addr[dev]) {
+    // The lookup makes the device's primary context current if none is.
     e = cudaGetSymbolAddress(&g_scratch_addr[dev], g_argmax_scratch);
     if (e != cudaSuccess) return e;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+    g_scratch_ctx[dev] = ctx;
   }
   *addr = g_scratch_addr[dev];
   return cudaSuccess;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
 
@@ -71,7 +101,7 @@ extern "C" int qmm_gemv_argmax_noalloc(const float *x, const uint32_t *codes, co
   if (!x || !codes || !scales || !idx) return QMM_ERR_ARG;
   if ((bits == 4) != (biases != nullptr)) return QMM_ERR_ARG;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (biases && !aligned16(biases)) ||
-      !aligned16(idx))
+      !aligned4(idx) || (val && !aligned4(val)))
     return QMM_ERR_ALIGN;
   void *scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return QMM_ERR_CUDA;

@@ -11,6 +11,7 @@ from quantized_weight_gb300 import qmm
 OK, ARG, SHAPE, ALIGN, UNSUP = 0, -1, -2, -3, -4
 FAKE = 0x10000          # never dereferenced: every call below fails validation first
 MIS = 0x10004           # not 16-byte aligned
+ODD = 0x10002           # not even 4-byte aligned
 
 
 @pytest.fixture(scope="module")
@@ -119,7 +120,9 @@ def test_argmax_validation(L):
     assert argmax(L, ws=None) == ARG
     assert argmax(L, b=None) == ARG
     assert argmax(L, ws=MIS) == ALIGN
-    assert argmax(L, i=MIS) == ALIGN
+    assert argmax(L, i=ODD) == ALIGN               # idx and val need only 4-byte alignment
+    assert argmax(L, v=ODD) == ALIGN
+    assert argmax(L, M=2, x=MIS, i=ODD) == ALIGN
     assert argmax(L, M=2, N=1000, nbytes=need - 1) == SHAPE   # workspace too small
 
 
