@@ -45,8 +45,9 @@
  * hardware", section "Build the execution path, then share the weights").
  *
  * Errors.  Each call returns a qmm_status.  Launch failures are QMM_ERR_CUDA.
- * The prefill kernel bounds every wait; if one runs out it records a device
- * status word and exits without writing its tile, and qmm_check() reports
+ * Every wait inside a kernel is bounded; if one runs out the kernel records
+ * a device status word, waits (bounded) for its own copies in flight, and
+ * exits without writing its output, and qmm_check() reports
  * QMM_ERR_DEVICE_TIMEOUT.  No exception crosses this interface.
  */
 #ifndef QMM_H
@@ -115,6 +116,18 @@ int qmm_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *
  *   Supported: bits 4 and 8 with group in {32, 64, 128}; bits 1 with group in
  *   {32, 64, 128} and K % 128 == 0.  K == 0 writes y = 0.
  *   M == 0 or N == 0 is a no-op.
+ *   Weight reads start early.  The decode kernels are launched as dependents
+ *   of the kernel before them on the stream (programmatic dependent launch):
+ *   they start copying codes, scales and biases while that kernel may still
+ *   run, and wait for it only before reading x.  A run of decode calls
+ *   (qmm_gemv, qmm_gemv_argmax, qmm_gemv_argmax_noalloc) back to back on one
+ *   stream can therefore overlap.  So the weights of a decode call must not
+ *   be written by the operation right before it on the stream, nor be the y
+ *   or argmax outputs of an earlier call of the same run.  Weights written on
+ *   the stream (qmm_pack, qmm_quantize, a copy) are safe once one operation
+ *   that is not a decode call (any other kernel or copy) or a host
+ *   synchronization lies between the write and the decode call.  x and y
+ *   follow plain stream order.
  */
 int qmm_gemv(const float *x, const uint32_t *codes, const uint16_t *scales,
              const uint16_t *biases, float *y, int64_t M, int64_t N, int64_t K, int bits,
@@ -130,7 +143,7 @@ int qmm_gemv(const float *x, const uint32_t *codes, const uint16_t *scales,
  *   projections: dequantize, then call the vendor"), and of the Q1 page's
  *   expand-to-FP32 prefill ("A 27B model on two 4GB Maxwell GPUs", section "A
  *   packed Q1 prefill kernel with a narrow dispatch window").
- *   Supported: bits 4, 8 and 1, group in {64, 128}, K % 64 == 0 (K % 128 == 0
+ *   Supported: bits 4, 8 and 1, group in {32, 64, 128}, K % 64 == 0 (K % 128 == 0
  *   for bits 1), K >= 64.  M == 0 or N == 0 is a no-op.
  */
 int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales,
@@ -223,10 +236,26 @@ int qmm_gather_dequant(const int32_t *ids, int64_t T, const uint32_t *packed, co
 
 /*
  * qmm_check -- synchronize `stream`, then report QMM_ERR_CUDA if a kernel
- * failed, QMM_ERR_DEVICE_TIMEOUT if a bounded wait in a prefill kernel ran
- * out since the last qmm_check (and clear that record), else QMM_OK.
+ * failed, QMM_ERR_DEVICE_TIMEOUT if a bounded wait in any kernel ran out
+ * since the last qmm_check (and clear that record), else QMM_OK.
  */
 int qmm_check(qmm_stream_t stream);
+
+/*
+ * qmm_test_timeout_next_decode -- test hook for the failure path above.  The
+ *   next decode launch that runs on the tensor-core decode kernel (qmm_gemv
+ *   or the argmax heads; every supported INT4 shape runs there) has its first
+ *   consumer warp wait on a barrier that is never completed, with a limit of
+ *   limit_ns instead of the normal 2 s.  That wait runs out: the launch
+ *   writes no output (an argmax head writes idx = 2147483647 and val =
+ *   -inf, no valid winner, and leaves its workspace ready), waits for its
+ *   copies in flight, and the next qmm_check() returns QMM_ERR_DEVICE_TIMEOUT;
+ *   the call after it runs normally.  One-shot: the launch that takes the
+ *   hook clears it.  limit_ns must be in [1000, 100000000] (QMM_ERR_ARG
+ *   otherwise).  Not for production use: it exists so that the timeout path
+ *   can be exercised without faulting or hanging a GPU.
+ */
+int qmm_test_timeout_next_decode(int64_t limit_ns);
 
 /* A static, human-readable name for a qmm_status value. */
 const char *qmm_status_string(int status);

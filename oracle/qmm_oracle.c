@@ -205,15 +205,22 @@ int oracle_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_
 
 /* ------------------------------------------------------------ the product */
 
+/* Row n of W decoded into wrow[0..K). */
+static void decode_row(double *wrow, const uint32_t *packed, const uint16_t *scales,
+                       const uint16_t *biases, int64_t n, int64_t K, int bits, int group)
+{
+    for (int64_t k = 0; k < K; k++)
+        wrow[k] = weight_at(packed, scales, biases, n, k, K, bits, group);
+}
+
 /* One output: acc = sum over groups g, over k in the group, of w[n,k]*x[m,k],
- * in double, in increasing k. */
-static double dot_one(const double *xrow, const uint32_t *packed, const uint16_t *scales,
-                      const uint16_t *biases, int64_t n, int64_t K, int bits, int group)
+ * in double, in increasing k (wrow: row n of W, decoded). */
+static double dot_row(const double *wrow, const double *xrow, int64_t K, int group)
 {
     double acc = 0.0;
     for (int64_t g0 = 0; g0 < K; g0 += group)
         for (int64_t k = g0; k < g0 + group; k++)
-            acc += weight_at(packed, scales, biases, n, k, K, bits, group) * xrow[k];
+            acc += wrow[k] * xrow[k];
     return acc;
 }
 
@@ -225,15 +232,19 @@ typedef struct {
     int64_t M, N, K;
     int bits, group;
     int64_t n_begin, n_end;
+    double *wrow;               /* [K] this thread's decoded row */
 } qmm_job;
 
+/* Row n is decoded once and used for every token m (each weight is the
+ * same value for every token, so this changes no result). */
 static void *qmm_worker(void *arg)
 {
     qmm_job *j = (qmm_job *)arg;
-    for (int64_t n = j->n_begin; n < j->n_end; n++)
+    for (int64_t n = j->n_begin; n < j->n_end; n++) {
+        decode_row(j->wrow, j->packed, j->scales, j->biases, n, j->K, j->bits, j->group);
         for (int64_t m = 0; m < j->M; m++)
-            j->y[m * j->N + n] = dot_one(j->x + m * j->K, j->packed, j->scales, j->biases, n,
-                                         j->K, j->bits, j->group);
+            j->y[m * j->N + n] = dot_row(j->wrow, j->x + m * j->K, j->K, j->group);
+    }
     return NULL;
 }
 
@@ -250,9 +261,11 @@ static int qmm_double_x(const double *x, const uint32_t *packed, const uint16_t 
     if (nthreads > N) nthreads = (int)(N > 0 ? N : 1);
     pthread_t tid[256];
     qmm_job jobs[256];
+    double *rows = (double *)malloc(sizeof(double) * (size_t)nthreads * (size_t)(K > 0 ? K : 1));
+    if (!rows) return -3;
     for (int t = 0; t < nthreads; t++) {
         jobs[t] = (qmm_job){x, packed, scales, biases, y, M, N, K, bits, group,
-                            N * t / nthreads, N * (t + 1) / nthreads};
+                            N * t / nthreads, N * (t + 1) / nthreads, rows + (size_t)t * (size_t)(K > 0 ? K : 1)};
     }
     int started = 0;
     for (int t = 1; t < nthreads; t++) {
@@ -262,6 +275,7 @@ static int qmm_double_x(const double *x, const uint32_t *packed, const uint16_t 
     qmm_worker(&jobs[0]);
     for (int t = 1; t <= started; t++) pthread_join(tid[t], NULL);
     for (int t = started + 1; t < nthreads; t++) qmm_worker(&jobs[t]);  /* threads that failed to start */
+    free(rows);
     return 0;
 }
 
@@ -303,15 +317,17 @@ int oracle_qmm_sampled(const void *x, int x_is_bf16, const uint32_t *packed,
 {
     if (!shape_ok(N, K, bits, group) || M < 0 || count < 0) return -1;
     if (bits == 4 && biases == NULL) return -1;
-    double *xrow = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    double *xrow = (double *)malloc(sizeof(double) * 2 * (size_t)(K > 0 ? K : 1));
     if (!xrow) return -3;
+    double *wrow = xrow + (K > 0 ? K : 1);
     for (int64_t i = 0; i < count; i++) {
         int64_t m = ms[i], n = ns[i];
         if (m < 0 || m >= M || n < 0 || n >= N) { free(xrow); return -2; }
         for (int64_t k = 0; k < K; k++)
             xrow[k] = x_is_bf16 ? oracle_bf16_to_double(((const uint16_t *)x)[m * K + k])
                                 : (double)((const float *)x)[m * K + k];
-        out[i] = dot_one(xrow, packed, scales, biases, n, K, bits, group);
+        decode_row(wrow, packed, scales, biases, n, K, bits, group);
+        out[i] = dot_row(wrow, xrow, K, group);
     }
     free(xrow);
     return 0;

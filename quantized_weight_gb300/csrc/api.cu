@@ -102,7 +102,6 @@ int qmm_gemv(const float *x, const uint32_t *codes, const uint16_t *scales, cons
 int qmm_gemm(const uint16_t *x_bf16, const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
              float *y, int64_t M, int64_t N, int64_t K, int bits, int group, qmm_stream_t stream) {
   if (!bits_ok(bits) || !group_ok(group)) return QMM_ERR_UNSUPPORTED;
-  if (group < 64) return QMM_ERR_UNSUPPORTED;
   if (M < 0 || N < 0 || K < 64 || K % 64 != 0 || K % group != 0 || M >= kMaxDim || N >= kMaxDim ||
       K >= kMaxDim)
     return QMM_ERR_SHAPE;
@@ -169,6 +168,12 @@ int qmm_gather_dequant(const int32_t *ids, int64_t T, const uint32_t *packed, co
   if (st != QMM_OK) return st;
   if (!aligned16(ids) || !aligned16(packed) || !aligned16(out)) return QMM_ERR_ALIGN;
   return cuda_status(qmm::launch_gather_dequant(ids, T, packed, scales, biases, out, N, K, bits, group, stream));
+}
+
+int qmm_test_timeout_next_decode(int64_t limit_ns) {
+  if (limit_ns < 1000 || limit_ns > 100000000) return QMM_ERR_ARG;
+  qmm::set_tc_test_wait((unsigned long long)limit_ns);
+  return QMM_OK;
 }
 
 int qmm_check(qmm_stream_t stream) {

@@ -26,13 +26,18 @@ struct WaitCtl {
 // the wait ran out of time (which then aborts the CTA and records the status).
 // A waiting thread sleeps inside try_wait (woken when the phase completes), so
 // waiting warps take no issue slots from the warps doing work.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl &c) {
+// `limit_ns` shorter than kWaitLimitNs serves only the test hook that makes a
+// wait run out on purpose.  With `stop_on_abort` false the wait ignores the
+// CTA's abort flag (it still gives up at the limit): for the thread that
+// issued the copies being waited for, which must not exit before they land.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl &c,
+                                             uint64_t limit_ns = kWaitLimitNs, bool stop_on_abort = true) {
   if (sm100::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = sm100::globaltimer_ns();
   for (;;) {
     if (sm100::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
-    if (*c.abort) return false;
-    if (sm100::globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (stop_on_abort && *c.abort) return false;
+    if (sm100::globaltimer_ns() - t0 > limit_ns) {
       *c.abort = 1;
       atomicExch(c.status, kTimeoutStatus);
       return false;

@@ -239,11 +239,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_2d(c_buf(s), &tmap_codes, cx, nb * BM, full(s));
         }
       }
-      if (!ok) {
-        // drain: every copy this thread issued must land before the CTA exits
-        const int first = it > STAGES ? it - STAGES : 0;
-        for (int j = first; j < it; j++) wait_drain(full(j % STAGES), (j / STAGES) & 1);
-      }
+      // drain: every copy this thread issued lands before it exits, also when
+      // the consumers give up later (after a normal run these waits end at once)
+      const int first = it > STAGES ? it - STAGES : 0;
+      for (int j = first; j < it; j++) wait_drain(full(j % STAGES), (j / STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -342,7 +341,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (UN > 1 && kb >= ksteps) break;
         const int s = ring.s;
         const uint32_t ph = ring.ph;
-        const int g = (kb * BK) >> p.gshift;
+        const int g = (kb * BK + 32 * part) >> p.gshift;  // this thread's 32 k lie in one group
         uint16_t sb = 0, bb = 0;
         if (G64) {
           if (row_ok) {

@@ -322,11 +322,10 @@ __global__ void __launch_bounds__(WIDE ? 896 : 512, (WIDE || MT > 1) ? 1 : 2)
         mbar_arrive(coef_full);                                  // the coefficients come with the stages
       }
       int j = 0;
-      bool ok = true;
       for (; j < nst; j++) {
         const int s = j % S;
         const uint32_t ph = (j / S) & 1;
-        if (!wait_bounded(empty(s), ph ^ 1, ctl)) { ok = false; break; }
+        if (!wait_bounded(empty(s), ph ^ 1, ctl)) break;
         const int r0 = j * p.stage_rows;
         const int nr = min(p.stage_rows, rows - r0);
         const uint32_t cbytes = (uint32_t)nr * p.row_bytes;
@@ -342,10 +341,10 @@ __global__ void __launch_bounds__(WIDE ? 896 : 512, (WIDE || MT > 1) ? 1 : 2)
                       gbytes, full(s), pol);
         }
       }
-      if (!ok) {
-        const int first = j > S ? j - S : 0;
-        for (int i = first; i < j; i++) wait_drain(full(i % S), (i / S) & 1);
-      }
+      // every copy this thread issued lands before it exits, also when the
+      // consumers give up later (after a normal run these waits end at once)
+      const int first = j > S ? j - S : 0;
+      for (int i = first; i < j; i++) wait_drain(full(i % S), (i / S) & 1);
       wait_drain(coef_full, 0);
     }
     return;

@@ -60,6 +60,7 @@
 // aborts the CTA, drains its outstanding copies and records
 // QMM_ERR_DEVICE_TIMEOUT for qmm_check().
 #include <algorithm>
+#include <atomic>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -74,6 +75,9 @@
 namespace qmm {
 
 __device__ int g_tc_status = 0;
+
+// Test hook: the limit the next launch's test wait gets (0: no test wait).
+std::atomic<unsigned long long> g_tc_test_wait_ns{0};
 
 namespace {
 
@@ -116,9 +120,18 @@ struct TcParams {
   int pstr0, pstr1;          // bytes per MMA pair of B in column blocks 0 and 1 (16 * nact + 16)
   int off_b, off_xs, off_red, off_zero, off_bar, off_am, off_tw;
   ArgmaxWork am;
+  // Test hook, 0 in every normal launch: > 0 makes the first consumer warp
+  // wait on a barrier that never completes, with this limit in nanoseconds,
+  // so that the wait runs out and the launch reports a device timeout.
+  unsigned long long test_wait_ns;
 };
 
 // ---------------------------------------------------------------- helpers
+
+// The test hook's wait (out of line: it runs only when the hook is set).
+__device__ __noinline__ void test_wait(uint32_t never_bar, WaitCtl ctl, unsigned long long limit_ns) {
+  wait_bounded(never_bar, 0, ctl, limit_ns);
+}
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -288,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       mbar_init(bars + 8 * s, 1);
       mbar_init(bars + 8 * (S + s), nks);
     }
+    mbar_init(bars + 8 * (2 * S) + 8, 1);      // test hook: initialised, never arrived on
     *abort_flag = 0;
     *reinterpret_cast<uint4 *>(smem + p.off_zero) = make_uint4(0u, 0u, 0u, 0u);   // B of inactive lanes
     fence_mbar_init();
@@ -303,10 +317,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       // ------------------------------------------------ producer (ring of 16-row stages)
       if (lane == 0) {
         const uint64_t pol = policy_evict_first();
-        bool ok = true;
         int j = 0;
         for (int s = 0, ph = 0; j < ntiles; j++) {
-          if (j >= S && !wait_bounded(bars + 8 * (S + s), ph ^ 1, ctl)) { ok = false; break; }
+          if (j >= S && !wait_bounded(bars + 8 * (S + s), ph ^ 1, ctl)) break;
           const uint32_t st = sbase + s * stage_bytes, fb = bars + 8 * s;
           mbar_arrive_expect_tx(fb, box_bytes);
           tma_load_3d_hint(st, &tm_codes, 0, n_begin + j * kTileRows, 0, fb, pol);
@@ -314,10 +327,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           if (FMT == 4) tma_load_3d_hint(st + code_bytes + coef_bytes, &tm_biases, 0, n_begin + j * kTileRows, 0, fb, pol);
           if (++s == S) s = 0, ph ^= 1;
         }
-        if (!ok) {
-          const int first = j > S ? j - S : 0;
-          for (int i = first; i < j; i++) wait_drain(bars + 8 * (i % S), (i / S) & 1);
-        }
+        // the last copies of every slot land before this thread exits (so
+        // that a CTA whose consumers gave up never exits with a copy in
+        // flight); after a normal run these waits end at once
+        const int first = j > S ? j - S : 0;
+        for (int i = first; i < j; i++) wait_drain(bars + 8 * (i % S), (i / S) & 1);
       }
       return;
     }
@@ -342,12 +356,14 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   const int g = lane >> 2, t = lane & 3;
   const int total_steps = ntiles * spt;
   const int W = total_steps < 16 ? total_steps : 16;    // not wide: working warps
-  bool ok = true;
   // not wide: wait for the slab before the dependent-launch wait (its copies
   // were issued at the start; the wait overlaps the previous kernel's tail)
   const int sb = (wide || cw >= W) ? 0 : run_begin(cw, W, total_steps);
   const int se = (wide || cw >= W) ? 0 : run_begin(cw + 1, W, total_steps);
-  if (!wide) ok = __all_sync(0xffffffffu, wait_bounded(bars, 0, ctl));
+  // (warp 0 holds the thread that issued the slab's copies: its wait does not
+  // stop at an abort, so the CTA never exits with a copy in flight)
+  bool ok = true;
+  if (!wide) ok = __all_sync(0xffffffffu, wait_bounded(bars, 0, ctl, kWaitLimitNs, warp != 0));
   pdl_wait();                                                  // x is written by the previous kernel
 
   // ---------------------------------------------- activation preparation
@@ -713,6 +729,9 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     }
   }
 
+  // test hook: the first consumer warp waits on the barrier nothing completes;
+  // the wait runs out and raises the CTA's abort flag, so no output is written
+  if (p.test_wait_ns && cw == 0) test_wait(bars + 8 * (2 * S) + 8, ctl, p.test_wait_ns);
   // every consumer warp gets here; then one thread per output adds the
   // partial sums in a fixed order
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
@@ -1043,6 +1062,7 @@ cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t
   if (!encode_maps(p, codes, scales, biases, tc, ts, tb)) return cudaErrorNotSupported;
   p.x = x;
   p.y = y;
+  p.test_wait_ns = g_tc_test_wait_ns.exchange(0);
   return launch_tc<false>(bits, uw, M > 4 ? 2 : 1, p.gpm, tc, ts, tb, p, grid, smem, s);
 }
 
@@ -1058,8 +1078,11 @@ cudaError_t launch_gemv_tc_argmax(const float *x, const uint32_t *codes, const u
   p.x = x;
   p.y = nullptr;
   p.am = w;
+  p.test_wait_ns = g_tc_test_wait_ns.exchange(0);
   return launch_tc<true>(bits, uw, 1, p.gpm, tc, ts, tb, p, grid, smem, s);
 }
+
+void set_tc_test_wait(unsigned long long limit_ns) { g_tc_test_wait_ns.store(limit_ns); }
 
 cudaError_t read_clear_tc_status(int *status, cudaStream_t s) {
   int v = 0;

@@ -95,6 +95,9 @@ cudaError_t read_clear_gemm_status(int *status, cudaStream_t s);
 cudaError_t read_clear_gemv_status(int *status, cudaStream_t s);
 cudaError_t read_clear_q1_status(int *status, cudaStream_t s);
 cudaError_t read_clear_batch_status(int *status, cudaStream_t s);
+// Test hook: the next tensor-core decode launch makes one wait on a barrier
+// that never completes, limited to limit_ns, and so reports a device timeout.
+void set_tc_test_wait(unsigned long long limit_ns);
 cudaError_t read_clear_tc_status(int *status, cudaStream_t s);
 
 }  // namespace qmm

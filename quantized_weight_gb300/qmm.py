@@ -69,12 +69,13 @@ def lib():
             L.qmm_gemv_argmax.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, ctypes.c_size_t, vp]
             L.qmm_gemv_argmax_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, vp]
             L.qmm_check.argtypes = [vp]
+            L.qmm_test_timeout_next_decode.argtypes = [i64]
             L.qmm_status_string.argtypes = [i32]
             L.qmm_status_string.restype = ctypes.c_char_p
             L.qmm_abi_version.argtypes = []
             for f in ("qmm_pack", "qmm_unpack", "qmm_dequant", "qmm_gemv", "qmm_gemm", "qmm_quantize",
                       "qmm_gather_dequant", "qmm_gemv_argmax", "qmm_gemv_argmax_noalloc", "qmm_check",
-                      "qmm_abi_version"):
+                      "qmm_test_timeout_next_decode", "qmm_abi_version"):
                 getattr(L, f).restype = i32
             _lib = L
     return _lib
@@ -254,6 +255,13 @@ def gather_dequant(ids, packed, scales, biases, N, K, bits, group, out=None, str
     _call("qmm_gather_dequant", lib().qmm_gather_dequant(_ptr(ids), T, _ptr(packed), _ptr(scales), _ptr(biases),
                                                          _ptr(out), N, K, bits, group, _stream(stream)))
     return out
+
+
+def test_timeout_next_decode(limit_ns: int) -> None:
+    """Test hook: the next tensor-core decode launch makes one wait that runs
+    out after limit_ns; it writes no output and the next check() raises
+    QMM_ERR_DEVICE_TIMEOUT."""
+    _call("qmm_test_timeout_next_decode", lib().qmm_test_timeout_next_decode(int(limit_ns)))
 
 
 def check(stream=None) -> None:

@@ -70,7 +70,7 @@ def test_gemm_validation(L):
     assert gemm(L, bits=2, b=None) == UNSUP
     assert gemm(L, bits=8, b=FAKE) == ARG          # INT8 takes no biases
     assert gemm(L, bits=1, b=None, K=192) == SHAPE  # Q1 prefill needs K % 128
-    assert gemm(L, g=32) == UNSUP
+    assert gemm(L, g=16) == UNSUP
     assert gemm(L, K=32) == SHAPE
     assert gemm(L, K=96) == SHAPE
     assert gemm(L, K=192, g=128) == SHAPE
@@ -105,6 +105,12 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 def argmax(L, x=FAKE, c=FAKE, s=FAKE, b=FAKE, i=FAKE, v=FAKE, M=1, N=64, K=128, bits=4, g=64, ws=FAKE,
            nbytes=1 << 20):
     return L.qmm_gemv_argmax(x, c, s, b, i, v, M, N, K, bits, g, ws, nbytes, None)
+
+
+def test_timeout_hook_validation(L):
+    assert L.qmm_test_timeout_next_decode(999) == ARG            # out of [1 us, 100 ms]
+    assert L.qmm_test_timeout_next_decode(100_000_001) == ARG
+    assert L.qmm_test_timeout_next_decode(-5) == ARG
 
 
 def test_argmax_validation(L):

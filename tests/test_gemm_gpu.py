@@ -28,6 +28,9 @@ SHAPES = [  # M, N, K, group: single and several tiles, ragged M and N, every BN
     # tiles wider than 256 (two MMAs per k-slice into one accumulator), the last with a ragged
     # second half
     (700, 7000, 1024, 64), (513, 5000, 512, 128), (1000, 6144, 128, 64), (300, 19456, 128, 64),
+    # group 32: two groups per 64-k step (each dequantizing thread's 32 k in one group), with a
+    # group count that is a multiple of 8 (vector coefficient loads) and one that is not
+    (129, 1000, 512, 32), (7, 200, 320, 32), (513, 2000, 1024, 32),
 ]
 
 
@@ -49,6 +52,7 @@ FORMATS = [  # M, N, K, bits, group: INT8 and Q1 codes through the same tensor-c
     (1, 128, 128, 8, 64), (100, 300, 1024, 8, 128), (513, 1024, 2048, 8, 64), (700, 7000, 1024, 8, 64),
     (1, 128, 128, 1, 128), (129, 1000, 512, 1, 64), (300, 130, 256, 1, 128), (1024, 2048, 5120, 1, 128),
     (1000, 6144, 256, 1, 128),   # Q1 where INT4 and INT8 would take token tiles wider than 256
+    (100, 300, 1024, 8, 32), (300, 1000, 320, 8, 32), (129, 1000, 512, 1, 32),   # group 32
 ]
 
 
@@ -88,6 +92,51 @@ def test_full_size_sampled(qmm, oracle_mod, name):
     y2 = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, w.bits, w.group)
     import torch
     assert torch.equal(y, y2)                    # same bits on every run
+
+
+def prefill_bound(d, bits, group, chunk=8192):
+    """Element-wise error bound of the prefill product against the exact one
+    on the same bf16 x: each weight is computed in float32 and rounded to
+    bfloat16 (relative error <= 2^-9 + 2^-24, taken as 2^-8), the products of
+    two bf16 values are exact in float32, and the float32 accumulation over K
+    adds at most (K + 16) * 2^-23 (twice the sequential-sum bound, for the
+    tensor core's accumulation order), all relative to sum_k |w_k| |x_k| with
+    |w| <= |s| q + |b|.  Independent of the oracle; rows of W in chunks."""
+    # a bf16 bit pattern is the upper half of the float32 with the same value
+    ax = np.abs((d["x_bf16"].astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    N, K = d["codes"].shape
+    out = np.empty((ax.shape[0], N))
+    for n0 in range(0, N, chunk):
+        sl = slice(n0, min(N, n0 + chunk))
+        sc = np.abs(d["scales"][sl].view(np.float16).astype(np.float64)).repeat(group, axis=1)
+        c = d["codes"][sl]
+        if bits == 4:
+            mag = sc * c + np.abs(d["biases"][sl].view(np.float16).astype(np.float64)).repeat(group, axis=1)
+        elif bits == 8:
+            mag = sc * np.abs(c.view(np.int8).astype(np.float64))
+        else:
+            mag = sc
+        out[:, sl] = ax @ mag.T
+    return (2.0 ** -8 + (K + 16) * 2.0 ** -23) * out
+
+
+# Every output of the full-size prefill shapes (the MLP up-projection at 1024
+# tokens in INT4 and INT8, and 256 tokens through the tied 151936-row head)
+# against the oracle's FP64 product on all host cores.
+@pytest.mark.parametrize("name", ["prefill_int4_m1024_k2048_n6144", "prefill_int8_m1024_k2048_n6144",
+                                  "prefill_int4_m256_k2048_n151936"])
+def test_full_size_every_output(qmm, oracle_mod, name):
+    w = inputs.WORKLOADS[name]
+    d = inputs.make_workload(name)
+    t = to_device(d, w.bits, with_bf16=True)
+    p = qmm.pack(t["codes"], w.bits)
+    y = qmm.gemm(t["x_bf16"], p, t["scales"], t["biases"], w.N, w.bits, w.group)
+    qmm.check()
+    y = y.cpu().numpy().astype(np.float64)
+    ref = oracle_mod.qmm_bf16x(d["x_bf16"], oracle_mod.pack(d["codes"], w.bits), d["scales"], d["biases"],
+                               w.N, w.K, w.bits, w.group)
+    assert rel_l2_rows(y, ref) <= TOL
+    assert np.all(np.abs(y - ref) <= prefill_bound(d, w.bits, w.group))
 
 
 def torch_index(a):

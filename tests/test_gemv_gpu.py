@@ -80,8 +80,9 @@ DECODE = ["decode_int4_k1024_n1024", "decode_int4_up_k2048_n6144", "decode_int4_
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_full_size_workloads(qmm, oracle_mod, name, seed):
     w = inputs.WORKLOADS[name]
-    y, ref, t, p, _ = run_case(qmm, oracle_mod, w.M, w.N, w.K, w.bits, w.group, seed)
+    y, ref, t, p, d = run_case(qmm, oracle_mod, w.M, w.N, w.K, w.bits, w.group, seed)
     assert rel_l2_rows(y, ref) <= TOL, name
+    assert np.all(np.abs(y - ref) <= fp32_bound(d, w.bits, w.group)), name
     # fixed reduction order: the same call gives the same bits
     y2 = qmm.gemv(t["x"], p, t["scales"], t["biases"], w.N, w.bits, w.group).cpu().numpy()
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
