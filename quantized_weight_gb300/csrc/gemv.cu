@@ -403,6 +403,12 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
     cudaError_t e = launch_gemv_q1(x, codes, scales, y, N, K, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
+  if (M >= 2 && ((bits == 8 && M >= 5) || bits == 1)) {
+    // 8-bit codes with 5 to 8 tokens and binary codes with 2 to 8 tokens: the
+    // tensor-core kernel with K split over a cluster (measured faster)
+    cudaError_t e = launch_gemv_tc(x, codes, scales, biases, y, M, N, K, bits, group, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (M >= 2 && M <= 8 && bits == 8) {
     // INT8, 2-8 tokens: the streamed kernel unpacks each code once per pass of up to four
     cudaError_t e = launch_gemv_stream(x, codes, scales, biases, y, M, N, K, bits, group, s);

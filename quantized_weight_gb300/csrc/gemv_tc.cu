@@ -120,6 +120,13 @@ struct TcParams {
   int pstr0, pstr1;          // bytes per MMA pair of B in column blocks 0 and 1 (16 * nact + 16)
   int off_b, off_xs, off_red, off_zero, off_bar, off_am, off_tw;
   ArgmaxWork am;
+  // K split over a cluster of ks CTAs (wide only; 1: no split).  Rank r of a
+  // cluster takes the slice of row_words words (NG groups) starting at word
+  // r * row_words of every row of the cluster's rows: all the sizes above
+  // are those of one slice.  K is the full length (x's row stride).
+  int ks;
+  int rmax;                  // rows of the largest cluster row block (its reduction buffer's stride)
+  int off_cl;                // shared offset of the reduction buffer (rank 0's is used)
   // Test hook, 0 in every normal launch: > 0 makes the first consumer warp
   // wait on a barrier that never completes, with this limit in nanoseconds,
   // so that the wait runs out and the launch reports a device timeout.
@@ -203,7 +210,9 @@ __device__ __forceinline__ void lds_codes(const uint8_t *smem, int rowb, int col
                                           uint32_t (&w)[UW]) {
   const uint8_t *lb = smem + (rowb + (word0 >> 5) * colstride);
   const int ch = (word0 >> 2) & 7;
-  if constexpr (UW == 2) {
+  if constexpr (UW == 1) {
+    w[0] = *reinterpret_cast<const uint32_t *>(lb + ((ch ^ sw) << 4) + (word0 & 3) * 4);
+  } else if constexpr (UW == 2) {
     const uint2 v = *reinterpret_cast<const uint2 *>(lb + ((ch ^ sw) << 4) + (word0 & 3) * 4);
     w[0] = v.x;
     w[1] = v.y;
@@ -249,7 +258,7 @@ __host__ __device__ __forceinline__ int last_warp(int tile, int spt, int W, int 
   return (W * ((tile + 1) * spt) + total - 1) / total - 1;
 }
 
-template <int FMT, int UW, int MT, int GPM, bool ARGMAX>
+template <int FMT, int UW, int MT, int GPM, bool ARGMAX, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_biases, const TcParams p) {
@@ -284,10 +293,14 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // not wide: 8-row blocks split over the CTAs; wide: the CTA's share of the rows
+  // (a cluster of ks CTAs shares one row block, each CTA a K slice)
+  const int ks = SPLIT ? p.ks : 1;
+  const int crank = SPLIT ? (int)cluster_ctarank() : 0;
   int n_begin, rows;
   if (wide) {
-    n_begin = (int)((int64_t)blockIdx.x * p.N / gridDim.x);
-    rows = (int)((int64_t)(blockIdx.x + 1) * p.N / gridDim.x) - n_begin;
+    const int ncl = gridDim.x / ks, cl = blockIdx.x / ks;
+    n_begin = (int)((int64_t)cl * p.N / ncl);
+    rows = (int)((int64_t)(cl + 1) * p.N / ncl) - n_begin;
   } else {
     const int o0 = (int)((int64_t)blockIdx.x * p.noct / gridDim.x);
     const int o1 = (int)((int64_t)(blockIdx.x + 1) * p.noct / gridDim.x);
@@ -322,9 +335,11 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
           if (j >= S && !wait_bounded(bars + 8 * (S + s), ph ^ 1, ctl)) break;
           const uint32_t st = sbase + s * stage_bytes, fb = bars + 8 * s;
           mbar_arrive_expect_tx(fb, box_bytes);
-          tma_load_3d_hint(st, &tm_codes, 0, n_begin + j * kTileRows, 0, fb, pol);
-          tma_load_3d_hint(st + code_bytes, &tm_scales, 0, n_begin + j * kTileRows, 0, fb, pol);
-          if (FMT == 4) tma_load_3d_hint(st + code_bytes + coef_bytes, &tm_biases, 0, n_begin + j * kTileRows, 0, fb, pol);
+          tma_load_3d_hint(st, &tm_codes, 0, n_begin + j * kTileRows, crank * (row_words >> 5), fb, pol);
+          tma_load_3d_hint(st + code_bytes, &tm_scales, 0, n_begin + j * kTileRows, crank * (NG >> 3), fb, pol);
+          if (FMT == 4)
+            tma_load_3d_hint(st + code_bytes + coef_bytes, &tm_biases, 0, n_begin + j * kTileRows, crank * (NG >> 3),
+                             fb, pol);
           if (++s == S) s = 0, ph ^= 1;
         }
         // the last copies of every slot land before this thread exits (so
@@ -332,6 +347,10 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         // flight); after a normal run these waits end at once
         const int first = j > S ? j - S : 0;
         for (int i = first; i < j; i++) wait_drain(bars + 8 * (i % S), (i / S) & 1);
+      }
+      if constexpr (SPLIT) {
+        __syncwarp();
+        cluster_sync();            // the consumers' cluster reduction (every thread takes part)
       }
       return;
     }
@@ -381,8 +400,18 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       float xv[NB][F::WPK];
 #pragma unroll
       for (int b = 0; b < NB; b++) {
-        const int u = base0 + b * nthreads + lane;
-        const float4 *src = reinterpret_cast<const float4 *>(p.x) + (int64_t)(u < total_words ? u : 0) * (F::WPK / 4);
+        // word u of the (token, slice word) sequence; a warp's 32 words lie in
+        // one token, whose slice starts at word crank * row_words of x's row
+        const int ub = base0 + b * nthreads;
+        int64_t xo = 0;                                            // float offset of word ub + lane
+        if (ub < total_words) {
+          xo = (int64_t)(ub + lane) * F::WPK;
+          if constexpr (SPLIT) {
+            const int mu = ub / row_words;
+            xo += (int64_t)mu * (p.K - row_words * F::WPK) + (int64_t)crank * row_words * F::WPK;
+          }
+        }
+        const float4 *src = reinterpret_cast<const float4 *>(p.x + xo);
 #pragma unroll
         for (int i = 0; i < F::WPK / 4; i++) {
           const float4 v = __ldg(src + i);
@@ -743,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       const int w1 = tw[2 * tile + 1];
       for (int w = tw[2 * tile]; w <= w1; w++) sum += red[((w + tile) * M + m) * kTileRows + rr];
     } else {
-      for (int ks = 0; ks < nks; ks++) sum += red[((tile * nks + ks) * M + m) * kTileRows + rr];
+      for (int q = 0; q < nks; q++) sum += red[((tile * nks + q) * M + m) * kTileRows + rr];
     }
     return sum;
   };
@@ -759,9 +788,39 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
     am_cta_finish(bv, bi, warp0, nwarps, reinterpret_cast<uint32_t *>(smem + p.off_am), 1, nthreads, p.am);
     return;
   }
-  if (!fin) return;
   float *__restrict__ y = p.y;
   const int N = p.N;
+  if constexpr (SPLIT) {
+    // K split over the cluster: ranks 1 .. ks-1 hand their row totals to
+    // rank 0 through distributed shared memory, with a flag saying whether
+    // they finished; rank 0 adds them in rank order (a fixed order) and stores
+    const uint32_t cbuf = sbase + p.off_cl;                 // [ks - 1][M][rmax] floats, then [ks - 1] flags
+    const int nbuf = (ks - 1) * M * p.rmax;
+    if (crank != 0) {
+      const uint32_t rb = mapa_shared(cbuf, 0);
+      for (int idx = ct; idx < rows * M; idx += nthreads) {
+        const int m = idx / rows, r = idx - m * rows;
+        st_cluster_f32(rb + 4u * (uint32_t)(((crank - 1) * M + m) * p.rmax + r), fin ? total(r, m) : 0.0f);
+      }
+      if (ct == 0) st_cluster_u32(rb + 4u * (uint32_t)(nbuf + crank - 1), fin ? 1u : 0u);
+    }
+    __syncwarp();
+    cluster_sync();
+    if (crank != 0) return;
+    const float *cb = reinterpret_cast<const float *>(smem + p.off_cl);
+    const uint32_t *cf = reinterpret_cast<const uint32_t *>(cb + nbuf);
+    bool all = fin;
+    for (int q = 1; q < ks; q++) all = all && cf[q - 1] != 0u;
+    if (!all) return;
+    for (int idx = ct; idx < rows * M; idx += nthreads) {
+      const int m = idx / rows, r = idx - m * rows;
+      float v = total(r, m);
+      for (int q = 1; q < ks; q++) v += cb[((q - 1) * M + m) * p.rmax + r];
+      y[(int64_t)m * N + n_begin + r] = v;
+    }
+    return;
+  }
+  if (!fin) return;
   if (M == 1) {
     for (int r = ct; r < rows; r += nthreads) y[n_begin + r] = total(r, 0);
   } else {
@@ -861,7 +920,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
 
   int best_uw = 0, best_wide = 0, best_S = 1, best_nks = 1, best_spt = 0;
   double best_cost = 1e30;
-  for (int uw = 8; uw >= 2; uw >>= 1) {
+  for (int uw = 8; uw >= 1; uw >>= 1) {
     if (wl % uw != 0 || !have_variant(fmt, uw, mt, gpm, argmax)) continue;
     const int spt = npos / uw;
     const double step_cost = uw * (1.0 + 0.15 * 8 / (uw * MPW));   // relative cost of one k-step
@@ -906,6 +965,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   }
   if (!best_uw) return false;
 
+  p.ks = 1;
   p.M = M;
   p.N = (int)N;
   p.K = (int)K;
@@ -965,6 +1025,122 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   return true;
 }
 
+// Two to eight tokens with K split over a cluster of ks CTAs: each CTA of a
+// cluster streams one K slice of the cluster's rows through a ring of 16-row
+// stages (wide layout, the sizes in p those of one slice); ncl clusters.
+bool plan_tc_split(int fmt, int M, int64_t N, int64_t K, int group, int ks, int ncl, TcParams &p, int &uw_out,
+                   int &grid, size_t &smem) {
+  const int WPK = fmt == 4 ? 8 : fmt == 8 ? 4 : 32;
+  const int MPW = fmt == 4 ? 2 : fmt == 8 ? 1 : 8;
+  if (M < 2 || M > 8 || ks < 2 || ks > 8 || ncl < 1) return false;
+  if (K % WPK != 0 || K % group != 0 || group % WPK != 0) return false;
+  const int NGf = (int)(K / group), rwf = (int)(K / WPK);
+  if (rwf % (32 * ks) != 0 || NGf % (8 * ks) != 0) return false;   // whole 128-byte columns and 8-group blocks
+  const int NG = NGf / ks, row_words = rwf / ks, wpg = group / WPK;
+  if (NG / 8 > 256 || row_words / 32 > 256 || wpg > 32) return false;
+  int gpm = 0;
+  if (M == 2 && NG % 2 == 0 && (wpg * 2) % 4 == 0) gpm = 2;
+  else if (wpg % 4 == 0) gpm = 1;
+  if (!gpm) return false;
+  const int mt = M > 4 ? 2 : 1;
+  if (mt == 2 && gpm != 1) return false;
+  const int wl = wpg * gpm / 4;
+  const int npos = row_words / 4;
+  const int row_bytes = (int)(K * (fmt == 4 ? 4 : fmt == 8 ? 8 : 1) / 8) / ks;
+  const int ncoef = fmt == 4 ? 2 : 1;
+  const int nact0 = gpm == 2 ? 16 : 8 * (M < 4 ? M : 4);
+  const int nact1 = M > 4 ? 8 * (M - 4) : 0;
+  const int nj2 = npos * MPW / 2;
+  const int pstr0 = nact0 * 16 + 16, pstr1 = nact1 ? nact1 * 16 + 16 : 0;
+  const size_t bbytes = (size_t)nj2 * (pstr0 + pstr1);
+  const size_t xsbytes = (size_t)M * NG * 16;
+  const int rmax = (int)((N + ncl - 1) / ncl);
+  const int nt_w = (rmax + kTileRows - 1) / kTileRows;
+  int uw = 0;
+  for (int c = 8; c >= 1 && !uw; c >>= 1)
+    if (wl % c == 0 && have_variant(fmt, c, mt, gpm, false)) uw = c;
+  if (!uw) return false;
+  const int spt = npos / uw;
+  // (tile, K slice) units go round robin to the 15 consumer warps: at least
+  // 15 units; a warp can wait on a stage up to 15 / nks tiles ahead of the
+  // oldest one still in use, so the ring holds 15 / nks + 3 stages (or every
+  // tile) for a stage's phase parity never to be taken for a later one
+  const size_t stage = align1k((size_t)kTileRows * row_bytes + (size_t)ncoef * kTileRows * NG * 2);
+  const size_t cl = ((size_t)(ks - 1) * M * rmax * 4 + 4 * (size_t)(ks - 1) + 15) & ~(size_t)15;
+  int nks = 1;
+  while (nt_w * nks < 15 && nks * 2 <= spt && spt % (nks * 2) == 0) nks *= 2;
+  int S = 0;
+  size_t red = 0;
+  for (;; nks *= 2) {
+    if (nks > spt || spt % nks != 0) return false;
+    red = (size_t)nt_w * nks * M * kTileRows * 4;
+    const size_t fixed = bbytes + xsbytes + red + 16 + 256 + kAmScratch + cl + 1024 + 64;
+    S = std::min(nt_w, 15 / nks + 3);
+    if (S * stage + fixed + 16 * (size_t)S <= (size_t)kSmemMax) break;
+  }
+
+  p = TcParams{};
+  p.ks = ks;
+  p.rmax = rmax;
+  p.M = M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.G = group;
+  p.NG = NG;
+  p.row_bytes = row_bytes;
+  p.row_words = row_words;
+  p.ncoef = ncoef;
+  p.gpm = gpm;
+  p.lg_gpm = ilog2(gpm);
+  p.lg_lpg = ilog2(4 / gpm);
+  p.wpg = wpg;
+  p.lg_wpg = ilog2(wpg);
+  p.wl = wl;
+  p.lg_wl = ilog2(wl);
+  p.npos = npos;
+  p.spt = spt;
+  p.wide = 1;
+  p.nks = nks;
+  p.lg_nks = ilog2(nks);
+  p.stages = S;
+  p.R = kTileRows;
+  p.BH = kTileRows;
+  p.noct = (int)((N + 7) / 8);
+  p.code_bytes = kTileRows * row_bytes;
+  p.coef_bytes = kTileRows * NG * 2;
+  p.stage_bytes = (int)stage;
+  p.warp0 = 1;
+  p.nwarps = 15;
+  p.nj2 = nj2;
+  p.nact0 = nact0;
+  p.nact1 = nact1;
+  p.pstr0 = pstr0;
+  p.pstr1 = pstr1;
+  size_t off = (size_t)S * stage;
+  p.off_b = (int)off;
+  off += bbytes;
+  p.off_xs = (int)off;
+  off += xsbytes;
+  p.off_red = (int)off;
+  off += red;
+  p.off_zero = (int)off;
+  off += 16;
+  p.off_tw = (int)off;
+  off += 8 * 32;
+  p.off_bar = (int)off;
+  off += 8 * 2 * S + 16;
+  off = (off + 15) & ~(size_t)15;
+  p.off_am = (int)off;
+  off += kAmScratch;
+  p.off_cl = (int)off;
+  off += cl;
+  smem = off + 1024;
+  if (smem > (size_t)kSmemMax) return false;
+  grid = ncl * ks;
+  uw_out = uw;
+  return true;
+}
+
 // Tensor maps of the codes (128-byte columns of R rows, 128-byte swizzle)
 // and of one coefficient array (8-group blocks of R rows).
 bool encode_maps(const TcParams &p, const void *codes, const void *scales, const void *biases, CUtensorMap &tc,
@@ -973,16 +1149,18 @@ bool encode_maps(const TcParams &p, const void *codes, const void *scales, const
   if (!enc) return false;
   const cuuint32_t es[3] = {1, 1, 1};
   {
-    cuuint64_t dims[3] = {32, (cuuint64_t)p.N, (cuuint64_t)(p.row_words / 32)};
-    cuuint64_t strides[2] = {(cuuint64_t)p.row_bytes, 128};
+    // (a K split copies one slice of every row: the box spans a slice, the
+    // tensor the full rows)
+    cuuint64_t dims[3] = {32, (cuuint64_t)p.N, (cuuint64_t)(p.ks * p.row_words / 32)};
+    cuuint64_t strides[2] = {(cuuint64_t)p.ks * p.row_bytes, 128};
     cuuint32_t box[3] = {32, (cuuint32_t)p.BH, (cuuint32_t)(p.row_words / 32)};
     if (enc(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(codes), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
-  cuuint64_t dims[3] = {8, (cuuint64_t)p.N, (cuuint64_t)(p.NG / 8)};
-  cuuint64_t strides[2] = {(cuuint64_t)p.NG * 2, 16};
+  cuuint64_t dims[3] = {8, (cuuint64_t)p.N, (cuuint64_t)(p.ks * p.NG / 8)};
+  cuuint64_t strides[2] = {(cuuint64_t)p.ks * p.NG * 2, 16};
   cuuint32_t box[3] = {8, (cuuint32_t)p.BH, (cuuint32_t)(p.NG / 8)};
   if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(scales), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -997,10 +1175,10 @@ bool encode_maps(const TcParams &p, const void *codes, const void *scales, const
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int UW, int MT, int GPM, bool ARGMAX>
+template <int FMT, int UW, int MT, int GPM, bool ARGMAX, bool SPLIT>
 cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUtensorMap &tb, const TcParams &p,
                          int grid, size_t smem, cudaStream_t s) {
-  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, ARGMAX>;
+  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, ARGMAX, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -1010,12 +1188,43 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (SPLIT) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.ks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, kern, tc, ts, tb, p);
+}
+
+// Clusters of ks CTAs of one kernel variant that fit on the GPU at once.
+template <int FMT, int UW, int MT, int GPM>
+int max_clusters_as(int ks, size_t smem) {
+  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 // The instantiated kernels: (format, k-step UW, column blocks MT, groups per
@@ -1026,7 +1235,7 @@ cudaError_t launch_tc(int fmt, int uw, int mt, int gpm, const CUtensorMap &tc, c
                       const CUtensorMap &tb, const TcParams &p, int grid, size_t smem, cudaStream_t s) {
 #define QMM_TC(F_, U_, T_, G_)                                                        \
   if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_)                                 \
-    return launch_tc_as<F_, U_, T_, G_, ARGMAX>(tc, ts, tb, p, grid, smem, s);
+    return launch_tc_as<F_, U_, T_, G_, ARGMAX, false>(tc, ts, tb, p, grid, smem, s);
   QMM_TC(4, 4, 1, 4) QMM_TC(4, 2, 1, 4)
   QMM_TC(8, 8, 1, 4) QMM_TC(8, 4, 1, 4)
   QMM_TC(1, 2, 1, 4)
@@ -1035,9 +1244,36 @@ cudaError_t launch_tc(int fmt, int uw, int mt, int gpm, const CUtensorMap &tc, c
     QMM_TC(8, 8, 1, 2) QMM_TC(8, 4, 1, 2)
     QMM_TC(4, 4, 1, 1) QMM_TC(4, 2, 1, 1) QMM_TC(4, 4, 2, 1) QMM_TC(4, 2, 2, 1)
     QMM_TC(8, 8, 1, 1) QMM_TC(8, 4, 1, 1) QMM_TC(8, 8, 2, 1) QMM_TC(8, 4, 2, 1)
+    QMM_TC(1, 2, 1, 2) QMM_TC(1, 1, 1, 2) QMM_TC(1, 1, 1, 1) QMM_TC(1, 1, 2, 1)
   }
 #undef QMM_TC
   return cudaErrorNotSupported;
+}
+
+// The K-split kernels (clusters of ks CTAs, two to eight tokens).
+cudaError_t launch_tc_split(int fmt, int uw, int mt, int gpm, const CUtensorMap &tc, const CUtensorMap &ts,
+                            const CUtensorMap &tb, const TcParams &p, int grid, size_t smem, cudaStream_t s) {
+#define QMM_TC(F_, U_, T_, G_) \
+  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_) return launch_tc_as<F_, U_, T_, G_, false, true>(tc, ts, tb, p, grid, smem, s);
+  QMM_TC(4, 4, 1, 2) QMM_TC(4, 2, 1, 2)
+  QMM_TC(8, 8, 1, 2) QMM_TC(8, 4, 1, 2)
+  QMM_TC(4, 4, 1, 1) QMM_TC(4, 2, 1, 1) QMM_TC(4, 4, 2, 1) QMM_TC(4, 2, 2, 1)
+  QMM_TC(8, 8, 1, 1) QMM_TC(8, 4, 1, 1) QMM_TC(8, 8, 2, 1) QMM_TC(8, 4, 2, 1)
+  QMM_TC(1, 2, 1, 2) QMM_TC(1, 1, 1, 2) QMM_TC(1, 1, 1, 1) QMM_TC(1, 1, 2, 1)
+#undef QMM_TC
+  return cudaErrorNotSupported;
+}
+
+int max_clusters(int fmt, int uw, int mt, int gpm, int ks, size_t smem) {
+#define QMM_TC(F_, U_, T_, G_) \
+  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_) return max_clusters_as<F_, U_, T_, G_>(ks, smem);
+  QMM_TC(4, 4, 1, 2) QMM_TC(4, 2, 1, 2)
+  QMM_TC(8, 8, 1, 2) QMM_TC(8, 4, 1, 2)
+  QMM_TC(4, 4, 1, 1) QMM_TC(4, 2, 1, 1) QMM_TC(4, 4, 2, 1) QMM_TC(4, 2, 2, 1)
+  QMM_TC(8, 8, 1, 1) QMM_TC(8, 4, 1, 1) QMM_TC(8, 8, 2, 1) QMM_TC(8, 4, 2, 1)
+  QMM_TC(1, 2, 1, 2) QMM_TC(1, 1, 1, 2) QMM_TC(1, 1, 1, 1) QMM_TC(1, 1, 2, 1)
+#undef QMM_TC
+  return 0;
 }
 
 bool have_variant(int fmt, int uw, int mt, int gpm, bool argmax) {
@@ -1046,6 +1282,7 @@ bool have_variant(int fmt, int uw, int mt, int gpm, bool argmax) {
   if (argmax) return false;
   if (fmt == 4) return (uw == 4 || uw == 2) && (gpm == 1 || mt == 1);
   if (fmt == 8) return (uw == 8 || uw == 4) && (gpm == 1 || mt == 1);
+  if (fmt == 1) return gpm == 2 ? mt == 1 && (uw == 2 || uw == 1) : uw == 1;
   return false;
 }
 
@@ -1057,12 +1294,37 @@ cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t
   TcParams p{};
   int uw = 0, grid = 0;
   size_t smem = 0;
-  if (!plan_tc(bits, M, N, K, group, false, p, uw, grid, smem)) return cudaErrorNotSupported;
+  bool planned = false;
+  // the K split is measured faster for 8-bit codes with 5 to 8 tokens and
+  // for binary codes; otherwise it is the fallback of the resident-slab plan
+  const bool split_first = (bits == 8 && M >= 5) || (bits == 1 && M >= 2);
+  if (M >= 2 && !split_first) planned = plan_tc(bits, M, N, K, group, false, p, uw, grid, smem);
+  if (M >= 2 && !planned) {
+    // K split over a cluster, slices of about 1024 k (the smallest split
+    // that gets there), on as many clusters as fit at once
+    const int sms = sm_count_tc();
+    for (int ks = 2; ks <= 8 && !planned; ks++) {
+      if (K / ks > 1024 && ks < 8) continue;
+      int ncl = sms / ks;
+      if (!plan_tc_split(bits, M, N, K, group, ks, ncl, p, uw, grid, smem)) continue;
+      const int fit = max_clusters(bits, uw, M > 4 ? 2 : 1, p.gpm, ks, smem);
+      if (fit < 1) continue;
+      if (fit < ncl) {
+        ncl = fit;
+        if (!plan_tc_split(bits, M, N, K, group, ks, ncl, p, uw, grid, smem)) continue;
+        if (max_clusters(bits, uw, M > 4 ? 2 : 1, p.gpm, ks, smem) < ncl) continue;
+      }
+      planned = true;
+    }
+  }
+  if (!planned && (M >= 2 && !split_first)) return cudaErrorNotSupported;
+  if (!planned && !plan_tc(bits, M, N, K, group, false, p, uw, grid, smem)) return cudaErrorNotSupported;
   CUtensorMap tc, ts, tb;
   if (!encode_maps(p, codes, scales, biases, tc, ts, tb)) return cudaErrorNotSupported;
   p.x = x;
   p.y = y;
   p.test_wait_ns = g_tc_test_wait_ns.exchange(0);
+  if (p.ks > 1) return launch_tc_split(bits, uw, M > 4 ? 2 : 1, p.gpm, tc, ts, tb, p, grid, smem, s);
   return launch_tc<false>(bits, uw, M > 4 ? 2 : 1, p.gpm, tc, ts, tb, p, grid, smem, s);
 }
 
