@@ -166,6 +166,26 @@ BATCH = [(2, 6144, 2048, 4, 64), (4, 6144, 2048, 4, 64), (8, 2048, 6144, 4, 64),
          (6, 40000, 1024, 8, 64), (2, 40000, 1024, 8, 64)]
 
 
+# two to eight tokens with K split over a cluster of ks CTAs (ks = K / 1024
+# rounded up to a whole split: 2, 3, 4, 5, 6, 8), each CTA a K slice of the
+# cluster's rows: many ring laps (40000 rows), clusters left with no rows
+# (N = 5), binary codes at the 27B FFN shape, and INT4 shapes whose resident
+# slab does not fit (the split is their fallback)
+SPLIT = [(8, 5, 4096, 8, 64), (5, 4000, 8192, 8, 64), (6, 3001, 2048, 8, 128), (7, 2333, 3072, 8, 64),
+         (2, 17408, 5120, 1, 128), (3, 4000, 5120, 1, 128), (8, 17408, 5120, 1, 128), (4, 7000, 4096, 1, 128),
+         (2, 3000, 2048, 1, 64), (8, 2048, 6144, 4, 64), (7, 1000, 6144, 4, 64)]
+
+
+@pytest.mark.parametrize("M,N,K,bits,group", SPLIT)
+def test_k_split_over_a_cluster(qmm, oracle_mod, M, N, K, bits, group):
+    y, ref, t, p, d = run_case(qmm, oracle_mod, M, N, K, bits, group, seed=M * N + K)
+    assert np.all(np.abs(y - ref) <= fp32_bound(d, bits, group)), (M, N, K, bits, group)
+    if N >= 32:
+        assert rel_l2_rows(y, ref) <= TOL
+    y2 = qmm.gemv(t["x"], p, t["scales"], t["biases"], N, bits, group).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))     # fixed order across the cluster
+
+
 # M = 1 slabs whose coefficients travel with each code stage (more than 16 KB
 # of coefficients per CTA), a ragged last stage included
 STAGED = [(40000, 1024, 4, 64), (40013, 1024, 4, 32), (41000, 4096, 8, 64)]
