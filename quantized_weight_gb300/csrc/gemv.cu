@@ -394,8 +394,11 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
   p.gshift = __builtin_ctz((unsigned)group);
   p.chunks_per_row = (int)(K * bits / 128);
   p.groups_per_row = (int)(K / group);
-  if (bits == 4) {
-    // INT4: the tensor-core kernel first (measured faster for every shape it takes)
+  if (bits == 4 && !(M == 1 && N * K <= ((int64_t)1 << 21))) {
+    // INT4: the tensor-core kernel first (measured faster for every shape it
+    // takes, except one-token products of at most 2 M weights: 1024 x 1024
+    // took 2.94 us there against 2.32 us on the streamed kernel, whose rows
+    // need no 16-row tiles)
     cudaError_t e = launch_gemv_tc(x, codes, scales, biases, y, M, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
@@ -422,8 +425,9 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
     cudaError_t e = launch_gemv_stream(x, codes, scales, biases, y, 1, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
-  if (bits != 4) {
-    // INT8 / Q1 shapes the kernels above do not take
+  {
+    // shapes the kernels above do not take (the same order as the fused
+    // argmax head for one token)
     cudaError_t e = launch_gemv_tc(x, codes, scales, biases, y, M, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
@@ -435,8 +439,9 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
 cudaError_t launch_gemv_argmax_fused(const float *x, const uint32_t *codes, const uint16_t *scales,
                                      const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
                                      const ArgmaxWork &w, cudaStream_t s) {
-  // the same kernel order as launch_gemv for one token
-  if (bits == 4) {
+  // the same kernel order as launch_gemv for one token (so that the winner's
+  // value equals that logit bit for bit)
+  if (bits == 4 && N * K > ((int64_t)1 << 21)) {
     const cudaError_t e = launch_gemv_tc_argmax(x, codes, scales, biases, N, K, bits, group, w, s);
     if (e != cudaErrorNotSupported) return e;
   }

@@ -430,22 +430,28 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         const bool valid = u < total_words;
         const int m = ubase / row_words;
         const int wd = u - m * row_words;
-        // the group's largest |x|
+        // the group's largest |x| and its sum, reduced in the same shuffle
+        // rounds; the sum of x' = 2^S x is the sum of x times 2^S (scaling by
+        // a power of two commutes with rounding away from over- and underflow)
         uint32_t mx = 0u;
-#pragma unroll
-        for (int e = 0; e < F::WPK; e++) mx = max(mx, absbits(xv[b][e]));
-        if (!valid) mx = 0u;
-        for (int o = 1; o < wpg; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const int Sx = scale_exp(mx);
-        const float sc = pow2f(Sx);
-        float wsum = 0.0f;
+        float rsum = 0.0f;
 #pragma unroll
         for (int e = 0; e < F::WPK; e++) {
-          xv[b][e] *= sc;
-          wsum += xv[b][e];
+          mx = max(mx, absbits(xv[b][e]));
+          rsum += xv[b][e];
         }
-        if (!valid) wsum = 0.0f;
-        for (int o = 1; o < wpg; o <<= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+        if (!valid) mx = 0u, rsum = 0.0f;
+        for (int o = 1; o < wpg; o <<= 1) {
+          const uint32_t om = __shfl_xor_sync(0xffffffffu, mx, o);
+          const float os = __shfl_xor_sync(0xffffffffu, rsum, o);
+          mx = max(mx, om);
+          rsum += os;
+        }
+        const int Sx = scale_exp(mx);
+        const float sc = pow2f(Sx);
+#pragma unroll
+        for (int e = 0; e < F::WPK; e++) xv[b][e] *= sc;
+        const float wsum = rsum * sc;
         if (!valid) continue;
         const int grp = wd >> lg_wpg, wig = wd & (wpg - 1);
         if (wig == 0) {
