@@ -71,6 +71,7 @@
 // QMM_ERR_DEVICE_TIMEOUT for qmm_check().
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -587,21 +588,26 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       for (int q = 0; q < NQ; q++) bf[cb][q] = lds128(smem + bofs0[cb] + (q0 + q) * bstr[cb]);
   };
 
-  // One k-step: UW words per lane starting at word0 of group grp (first:
-  // word0 is the lane's first word of the group), with B fragments bf and
-  // the group's constants xc, into acc.
-  auto step = [&](int word0, int grp, bool first, const uint4 (&bf)[MT][NQ], const float4 (&xc)[MT]) {
+  // One k-step: UW words per lane starting at word0, with B fragments bf,
+  // accumulated into d (zero: d starts from zero).  In the resident-slab
+  // layout the k-steps of a group accumulate into one d and step_epi applies
+  // the group's coefficients once: at the group's last step, or where a
+  // warp's run ends inside the group (the epilogue is linear in d; the x-only
+  // term goes with the part that holds the group's first step).  The ring
+  // layout, throughput-bound with many warps, keeps one epilogue per k-step
+  // (each step's MMA chains independent: measured faster there); `fresh`
+  // (a std::integral_constant) selects that at compile time.
+  auto step_mma = [&](int word0, const uint4 (&bf)[MT][NQ], float (&d)[2][MT][4], bool zero, auto fresh) {
+    constexpr bool FRESH = decltype(fresh)::value;
+    if (!FRESH && zero) {
+#pragma unroll
+      for (int h = 0; h < 2; h++)
+#pragma unroll
+        for (int cb = 0; cb < MT; cb++) d[h][cb][0] = d[h][cb][1] = d[h][cb][2] = d[h][cb][3] = 0.0f;
+    }
     uint32_t wa[UW], wb[UW];
     lds_codes<UW>(smem, ca, colstride, swa, word0, wa);
     lds_codes<UW>(smem, cb8, colstride, swb, word0, wb);
-    const int kofs = (grp >> 3) * kblk + (grp & 7) * 2;
-    const uint16_t sah = lds16(smem + ka + kofs), sbh = lds16(smem + kb8 + kofs);
-    uint16_t eah = 0, ebh = 0;
-    if (FMT == 4 && first) {
-      eah = lds16(smem + ka + coef_bytes + kofs);
-      ebh = lds16(smem + kb8 + coef_bytes + kofs);
-    }
-    float d[2][MT][4];
 #pragma unroll
     for (int u = 0; u < UW; u++) {
       if constexpr (FMT == 4) {
@@ -609,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 #pragma unroll
         for (int cb = 0; cb < MT; cb++) {
           const uint4 b = bf[cb][u];
-          if (u == 0) {
+          if (FRESH && u == 0) {
             mma_f16_z(d[0][cb], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
             mma_f16_z(d[1][cb], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
           } else {
@@ -624,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 #pragma unroll
           for (int cb = 0; cb < MT; cb++) {
             const uint4 b = bf[cb][u >> 1];
-            if (u == 0) {
+            if (FRESH && u == 0) {
               mma_f16_z(d[0][cb], prmt(w0, 0u, 0x4140u), prmt(v0, 0u, 0x4140u), prmt(w0, 0u, 0x4342u),
                         prmt(v0, 0u, 0x4342u), b.x, b.y);
               mma_f16_z(d[1][cb], prmt(w1, 0u, 0x4140u), prmt(v1, 0u, 0x4140u), prmt(w1, 0u, 0x4342u),
@@ -652,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
 #pragma unroll
           for (int cb = 0; cb < MT; cb++) {
             const uint4 b = bf[cb][4 * u + jp];
-            if (u == 0 && jp == 0) {
+            if (FRESH && u == 0 && jp == 0) {
               mma_f16_z(d[0][cb], aw[0], av[0], aw[1], av[1], b.x, b.y);
               mma_f16_z(d[1][cb], aw[2], av[2], aw[3], av[3], b.z, b.w);
             } else {
@@ -663,14 +669,23 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
         }
       }
     }
-    // epilogue: (s' D + e X) * 2^(24 - S) per (row, group, token), with the
-    // x-only correction e X once per group
+  };
+
+  // The coefficients of group grp applied to its accumulated d, into acc:
+  // (s' D + e X) * 2^(24 - S) per (row, group, token), the x-only
+  // correction e X only when withx.
+  auto step_epi = [&](int grp, bool withx, const float (&d)[2][MT][4]) {
+    const int kofs = (grp >> 3) * kblk + (grp & 7) * 2;
+    const uint16_t sah = lds16(smem + ka + kofs), sbh = lds16(smem + kb8 + kofs);
+    float4 xc[MT];
+#pragma unroll
+    for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tokofs[cb] + grp];
     float sa = h2f(sah), sbv = h2f(sbh);
     float ea = 0.0f, eb = 0.0f;
-    if (first) {
+    if (withx) {
       if constexpr (FMT == 4) {
-        ea = h2f(eah);
-        eb = h2f(ebh);
+        ea = h2f(lds16(smem + ka + coef_bytes + kofs));
+        eb = h2f(lds16(smem + kb8 + coef_bytes + kofs));
       } else if constexpr (FMT == 8) {
         ea = -128.0f * sa;
         eb = -128.0f * sbv;
@@ -694,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   };
 
   uint4 bf[MT][NQ];
-  float4 xc[MT];
+  float d[2][MT][4];
   if (!wide) {
     if (ok && se > sb) {
       int tile = sb / spt;
@@ -703,19 +718,24 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       int wi = pst & (wl - 1);
       int grp = ((pst >> lg_wl) << LG_GPM) + gsel_lane;
       int word0 = grp * wpg + wofs_lane + wi;
+      bool withx = wi == 0, zero = true;
       set_rows(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
       for (int s = sb; s < se; s++) {
         load_b(pst, bf);
-#pragma unroll
-        for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tokofs[cb] + grp];
-        step(word0, grp, wi == 0, bf, xc);
+        step_mma(word0, bf, d, zero, std::false_type{});
+        zero = false;
         pst += UW;
         wi += UW;
         word0 += UW;
+        if (wi == wl || s + 1 == se) {                          // the group's last step here
+          step_epi(grp, withx, d);
+          zero = true;
+        }
         if (wi == wl) {
           wi = 0;
           grp += GPM;
           word0 += GPM * wpg - wl;
+          withx = true;
         }
         if (pst == npos || s + 1 == se) {
           flush(cw + tile);                           // (warp, tile) -> warp + tile is one-to-one
@@ -747,9 +767,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       int word0 = grp * wpg + wofs_lane + wi;
       for (int s = 0; s < spu; s++) {
         load_b(pst, bf);
-#pragma unroll
-        for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tokofs[cb] + grp];
-        step(word0, grp, wi == 0, bf, xc);
+        step_mma(word0, bf, d, true, std::true_type{});
+        step_epi(grp, wi == 0, d);
         pst += UW;
         wi += UW;
         word0 += UW;

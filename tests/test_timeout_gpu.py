@@ -78,12 +78,12 @@ def test_the_hook_is_one_shot_and_rejects_out_of_range_limits(qmm):
         qmm.test_timeout_next_decode(10)
     with pytest.raises(qmm.QmmError):
         qmm.test_timeout_next_decode(10 ** 9)
-    d = inputs.make(1, 1024, 1024, 4, 64, seed=1)
+    d = inputs.make(1, 4096, 2048, 4, 64, seed=1)   # an INT4 shape of the tensor-core kernel
     t = to_device(d, 4)
     p = qmm.pack(t["codes"], 4)
     qmm.test_timeout_next_decode(200_000)
-    qmm.gemv(t["x"], p, t["scales"], t["biases"], 1024, 4, 64)
+    qmm.gemv(t["x"], p, t["scales"], t["biases"], 4096, 4, 64)
     expect_timeout(qmm)
     for _ in range(3):
-        qmm.gemv(t["x"], p, t["scales"], t["biases"], 1024, 4, 64)
+        qmm.gemv(t["x"], p, t["scales"], t["biases"], 4096, 4, 64)
     qmm.check()                   # the hook was taken by the first launch only
