@@ -253,8 +253,13 @@ __device__ __forceinline__ void b_lane(int gpm, int m, int t, int tau, int &cb, 
 // every run is non-empty.
 __host__ __device__ __forceinline__ int run_begin(int w, int W, int total) { return w * total / W; }
 
-template <int FMT, int UW, int MT, int GPM, bool ARGMAX, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
+// LAY: 0 resident slab (one-token kernels; the others also take a ring at
+// run time), 1 ring (one-token kernels for long slabs, whose shared memory
+// holds one CTA per SM: up to 128 registers), 2 ring with K split over a
+// cluster.  Separate instantiations keep each kernel's code to the
+// layout it runs (code a kernel carries but never runs measured 2 % slower).
+template <int FMT, int UW, int MT, int GPM, bool ARGMAX, int LAY>
+__global__ void __launch_bounds__(kThreads, MT == 1 && LAY != 1 ? 2 : 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_biases, const TcParams p) {
   using F = Fmt<FMT>;
@@ -266,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
   // the parameters the loops use, in registers
   const int M = p.M, NG = p.NG, row_words = p.row_words;
   const int wpg = p.wpg, lg_wpg = p.lg_wpg, wl = p.wl, lg_wl = p.lg_wl, npos = p.npos, spt = p.spt;
-  const bool wide = p.wide != 0;
+  constexpr bool SPLIT = LAY == 2;
+  const bool wide = LAY != 0 || (GPM != 4 && p.wide != 0);
   const int nks = p.nks, lg_nks = p.lg_nks, S = p.stages, stage_bytes = p.stage_bytes;
   const int code_bytes = p.code_bytes, coef_bytes = p.coef_bytes;
   const int nj2 = p.nj2, nwarps = p.nwarps, warp0 = p.warp0;
@@ -755,27 +761,54 @@ __global__ void __launch_bounds__(kThreads, MT == 1 ? 2 : 1)
       }
     }
   } else {
+    // Each ring slot has its own nks consumer warps (S * nks <= 15), and a
+    // warp takes its slot's tiles in order, so every wait is for the next
+    // phase of its own slot: a phase parity can never be taken for another
+    // lap (copies may land out of order)
     const int spu = spt >> lg_nks;                   // steps per unit
-    for (int u = cw; ok && u < ntiles * nks; u += nwarps) {
-      const int tile = u >> lg_nks, ks = u & (nks - 1);
-      const int slot = tile % S;
-      if (!__all_sync(0xffffffffu, wait_bounded(bars + 8 * slot, (tile / S) & 1, ctl))) { ok = false; break; }
+    const int slot = cw >> lg_nks, kq = cw & (nks - 1);   // the warp's slot and K slice
+    for (int tile = slot, lap = 0; ok && cw < S * nks && tile < ntiles; tile += S, lap ^= 1) {
+      const int u = tile * nks + kq;
+      if (!__all_sync(0xffffffffu, wait_bounded(bars + 8 * slot, lap, ctl))) { ok = false; break; }
       set_rows(slot * stage_bytes, g, g + 8);
-      int pst = ks * spu * UW;
+      int pst = kq * spu * UW;
       int wi = pst & (wl - 1);
       int grp = ((pst >> lg_wl) << LG_GPM) + gsel_lane;
       int word0 = grp * wpg + wofs_lane + wi;
-      for (int s = 0; s < spu; s++) {
-        load_b(pst, bf);
-        step_mma(word0, bf, d, true, std::true_type{});
-        step_epi(grp, wi == 0, d);
-        pst += UW;
-        wi += UW;
-        word0 += UW;
-        if (wi == wl) {
-          wi = 0;
+      if (GPM == 4 && wl == 2 * UW && wi == 0 && (spu & 1) == 0) {
+        // a group is two k-steps: each into its own accumulators (two
+        // independent MMA chains, as with an epilogue per step), added once,
+        // and one epilogue per group
+        float d2[2][MT][4];
+        for (int s = 0; s < spu; s += 2) {
+          load_b(pst, bf);
+          step_mma(word0, bf, d, true, std::true_type{});
+          load_b(pst + UW, bf);
+          step_mma(word0 + UW, bf, d2, true, std::true_type{});
+#pragma unroll
+          for (int h = 0; h < 2; h++)
+#pragma unroll
+            for (int cb = 0; cb < MT; cb++)
+#pragma unroll
+              for (int i = 0; i < 4; i++) d[h][cb][i] += d2[h][cb][i];
+          step_epi(grp, true, d);
+          pst += 2 * UW;
           grp += GPM;
-          word0 += GPM * wpg - wl;
+          word0 += GPM * wpg;
+        }
+      } else {
+        for (int s = 0; s < spu; s++) {
+          load_b(pst, bf);
+          step_mma(word0, bf, d, true, std::true_type{});
+          step_epi(grp, wi == 0, d);
+          pst += UW;
+          wi += UW;
+          word0 += UW;
+          if (wi == wl) {
+            wi = 0;
+            grp += GPM;
+            word0 += GPM * wpg - wl;
+          }
         }
       }
       flush(u);
@@ -969,24 +1002,25 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
         continue;
       }
     }
-    // ring of 16-row stages with a producer warp; 15 consumer warps take
-    // (tile, K slice) units round robin
+    // ring of 16-row stages with a producer warp; each of the S slots has
+    // nks consumer warps (S * nks <= 15) taking its tiles in order, one K
+    // slice each
     if (mt != 1) continue;
     const int rows_w = (int)((N + sms - 1) / sms);
     const int nt_w = (rows_w + kTileRows - 1) / kTileRows;
     const size_t stage = align1k((size_t)kTileRows * row_bytes + (size_t)ncoef * kTileRows * NG * 2);
-    for (int nks = 1; nks <= spt; nks <<= 1) {
+    for (int nks = 1; nks <= 8 && nks <= spt; nks <<= 1) {
       if (spt % nks) break;
-      const int ring = std::min(15 / nks + 3, nt_w);
+      const int ring = std::min(15 / nks, nt_w);
       const size_t smw = (size_t)ring * stage + bbytes + xsbytes + (size_t)nt_w * nks * M * kTileRows * 4 + misc +
                          16 * (size_t)ring;
       if (smw > (size_t)kSmemMax) continue;
-      const double c = (double)((nt_w * nks + 14) / 15) * (spt / nks) * step_cost * 16.0 / 15.0 *
+      // the longest warp: ceil(tiles / S) units of spt / nks steps
+      const double c = (double)((nt_w + ring - 1) / ring) * (spt / nks) * step_cost *
                        ((double)nt_w / std::max(1, ntiles));
       if (c < best_cost) {
         best_cost = c, best_uw = uw, best_wide = 1, best_S = ring, best_nks = nks, best_spt = spt;
       }
-      break;
     }
   }
   if (!best_uw) return false;
@@ -1087,23 +1121,22 @@ bool plan_tc_split(int fmt, int M, int64_t N, int64_t K, int group, int ks, int 
     if (wl % c == 0 && have_variant(fmt, c, mt, gpm, false)) uw = c;
   if (!uw) return false;
   const int spt = npos / uw;
-  // (tile, K slice) units go round robin to the 15 consumer warps: at least
-  // 15 units; a warp can wait on a stage up to 15 / nks tiles ahead of the
-  // oldest one still in use, so the ring holds 15 / nks + 3 stages (or every
-  // tile) for a stage's phase parity never to be taken for a later one
+  // each of the S ring slots has nks consumer warps (S * nks <= 15) taking
+  // its tiles in order; nks is chosen for the shortest longest warp
   const size_t stage = align1k((size_t)kTileRows * row_bytes + (size_t)ncoef * kTileRows * NG * 2);
   const size_t cl = ((size_t)(ks - 1) * M * rmax * 4 + 4 * (size_t)(ks - 1) + 15) & ~(size_t)15;
-  int nks = 1;
-  while (nt_w * nks < 15 && nks * 2 <= spt && spt % (nks * 2) == 0) nks *= 2;
-  int S = 0;
+  int nks = 0, S = 0;
   size_t red = 0;
-  for (;; nks *= 2) {
-    if (nks > spt || spt % nks != 0) return false;
-    red = (size_t)nt_w * nks * M * kTileRows * 4;
-    const size_t fixed = bbytes + xsbytes + red + 16 + 256 + kAmScratch + cl + 1024 + 64;
-    S = std::min(nt_w, 15 / nks + 3);
-    if (S * stage + fixed + 16 * (size_t)S <= (size_t)kSmemMax) break;
+  long best = 0;
+  for (int c = 1; c <= 8 && c <= spt && spt % c == 0; c <<= 1) {
+    const int sc = std::min(nt_w, 15 / c);
+    const size_t rc = (size_t)nt_w * c * M * kTileRows * 4;
+    const size_t fixed = bbytes + xsbytes + rc + 16 + 256 + kAmScratch + cl + 1024 + 64;
+    if (sc * stage + fixed + 16 * (size_t)sc > (size_t)kSmemMax) continue;
+    const long cost = (long)((nt_w + sc - 1) / sc) * (spt / c);
+    if (!nks || cost < best) nks = c, S = sc, red = rc, best = cost;
   }
+  if (!nks) return false;
 
   p = TcParams{};
   p.ks = ks;
@@ -1201,10 +1234,11 @@ bool encode_maps(const TcParams &p, const void *codes, const void *scales, const
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int UW, int MT, int GPM, bool ARGMAX, bool SPLIT>
+template <int FMT, int UW, int MT, int GPM, bool ARGMAX, int LAY>
 cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUtensorMap &tb, const TcParams &p,
                          int grid, size_t smem, cudaStream_t s) {
-  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, ARGMAX, SPLIT>;
+  constexpr bool SPLIT = LAY == 2;
+  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, ARGMAX, LAY>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -1232,7 +1266,7 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
 // Clusters of ks CTAs of one kernel variant that fit on the GPU at once.
 template <int FMT, int UW, int MT, int GPM>
 int max_clusters_as(int ks, size_t smem) {
-  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, false, true>;
+  auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, false, 2>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks);
@@ -1259,9 +1293,19 @@ int max_clusters_as(int ks, size_t smem) {
 template <bool ARGMAX>
 cudaError_t launch_tc(int fmt, int uw, int mt, int gpm, const CUtensorMap &tc, const CUtensorMap &ts,
                       const CUtensorMap &tb, const TcParams &p, int grid, size_t smem, cudaStream_t s) {
+  if (gpm == 4 && p.wide) {
 #define QMM_TC(F_, U_, T_, G_)                                                        \
   if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_)                                 \
-    return launch_tc_as<F_, U_, T_, G_, ARGMAX, false>(tc, ts, tb, p, grid, smem, s);
+    return launch_tc_as<F_, U_, T_, G_, ARGMAX, 1>(tc, ts, tb, p, grid, smem, s);
+    QMM_TC(4, 4, 1, 4) QMM_TC(4, 2, 1, 4)
+    QMM_TC(8, 8, 1, 4) QMM_TC(8, 4, 1, 4)
+    QMM_TC(1, 2, 1, 4)
+#undef QMM_TC
+    return cudaErrorNotSupported;
+  }
+#define QMM_TC(F_, U_, T_, G_)                                                        \
+  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_)                                 \
+    return launch_tc_as<F_, U_, T_, G_, ARGMAX, 0>(tc, ts, tb, p, grid, smem, s);
   QMM_TC(4, 4, 1, 4) QMM_TC(4, 2, 1, 4)
   QMM_TC(8, 8, 1, 4) QMM_TC(8, 4, 1, 4)
   QMM_TC(1, 2, 1, 4)
@@ -1280,7 +1324,7 @@ cudaError_t launch_tc(int fmt, int uw, int mt, int gpm, const CUtensorMap &tc, c
 cudaError_t launch_tc_split(int fmt, int uw, int mt, int gpm, const CUtensorMap &tc, const CUtensorMap &ts,
                             const CUtensorMap &tb, const TcParams &p, int grid, size_t smem, cudaStream_t s) {
 #define QMM_TC(F_, U_, T_, G_) \
-  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_) return launch_tc_as<F_, U_, T_, G_, false, true>(tc, ts, tb, p, grid, smem, s);
+  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_) return launch_tc_as<F_, U_, T_, G_, false, 2>(tc, ts, tb, p, grid, smem, s);
   QMM_TC(4, 4, 1, 2) QMM_TC(4, 2, 1, 2)
   QMM_TC(8, 8, 1, 2) QMM_TC(8, 4, 1, 2)
   QMM_TC(4, 4, 1, 1) QMM_TC(4, 2, 1, 1) QMM_TC(4, 4, 2, 1) QMM_TC(4, 2, 2, 1)
