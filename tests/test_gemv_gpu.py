@@ -186,6 +186,20 @@ def test_k_split_over_a_cluster(qmm, oracle_mod, M, N, K, bits, group):
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))     # fixed order across the cluster
 
 
+# The ring layouts on cold weights (every product reads fresh tensors, larger
+# than L2 together): copies into a ring slot may land out of order, which once
+# let a consumer take a slot's previous lap for its own.  Every output is
+# checked against the float32 bound.
+RING_COLD = [(1, 151936, 2048, 4, 64), (8, 4096, 4096, 8, 64), (2, 17408, 5120, 1, 128)]
+
+
+@pytest.mark.parametrize("M,N,K,bits,group", RING_COLD)
+def test_ring_layouts_on_cold_weights(qmm, oracle_mod, M, N, K, bits, group):
+    for seed in range(3):
+        y, ref, t, p, d = run_case(qmm, oracle_mod, M, N, K, bits, group, seed=100 + seed)
+        assert np.all(np.abs(y - ref) <= fp32_bound(d, bits, group)), (M, N, K, bits, group, seed)
+
+
 # M = 1 slabs whose coefficients travel with each code stage (more than 16 KB
 # of coefficients per CTA), a ragged last stage included
 STAGED = [(40000, 1024, 4, 64), (40013, 1024, 4, 32), (41000, 4096, 8, 64)]
