@@ -95,6 +95,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 512;              // 16 warps
+constexpr int kThreadsRing = 544;          // one-token ring: a producer warp and 16 consumer warps
 constexpr int kTileRows = 16;              // rows per MMA tile and per stage
 constexpr int kSmemMax = 225 * 1024;
 constexpr int kSmemPair = 113 * 1024;      // at most this much shared memory: two CTAs per SM
@@ -259,7 +260,7 @@ __host__ __device__ __forceinline__ int run_begin(int w, int W, int total) { ret
 // cluster.  Separate instantiations keep each kernel's code to the
 // layout it runs (code a kernel carries but never runs measured 2 % slower).
 template <int FMT, int UW, int MT, int GPM, bool ARGMAX, int LAY>
-__global__ void __launch_bounds__(kThreads, MT == 1 && LAY != 1 ? 2 : 1)
+__global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 && LAY != 1 ? 2 : 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_biases, const TcParams p) {
   using F = Fmt<FMT>;
@@ -1009,9 +1010,10 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
     const int rows_w = (int)((N + sms - 1) / sms);
     const int nt_w = (rows_w + kTileRows - 1) / kTileRows;
     const size_t stage = align1k((size_t)kTileRows * row_bytes + (size_t)ncoef * kTileRows * NG * 2);
+    const int consumers = gpm == 4 ? 16 : 15;     // one-token rings run with a 17th warp
     for (int nks = 1; nks <= 8 && nks <= spt; nks <<= 1) {
       if (spt % nks) break;
-      const int ring = std::min(15 / nks, nt_w);
+      const int ring = std::min(consumers / nks, nt_w);
       const size_t smw = (size_t)ring * stage + bbytes + xsbytes + (size_t)nt_w * nks * M * kTileRows * 4 + misc +
                          16 * (size_t)ring;
       if (smw > (size_t)kSmemMax) continue;
@@ -1054,7 +1056,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   p.coef_bytes = p.R * NG * 2;
   p.stage_bytes = (int)align1k((size_t)p.code_bytes + (size_t)ncoef * p.coef_bytes);
   p.warp0 = best_wide ? 1 : 0;
-  p.nwarps = best_wide ? 15 : 16;
+  p.nwarps = best_wide ? (gpm == 4 ? 16 : 15) : 16;
   p.nj2 = nj2;
   p.nact0 = nact0;
   p.nact1 = nact1;
@@ -1245,7 +1247,7 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(LAY == 1 ? kThreadsRing : kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
