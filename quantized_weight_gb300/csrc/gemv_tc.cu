@@ -71,6 +71,7 @@
 // QMM_ERR_DEVICE_TIMEOUT for qmm_check().
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include <cuda.h>
@@ -1241,10 +1242,20 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
                          int grid, size_t smem, cudaStream_t s) {
   constexpr bool SPLIT = LAY == 2;
   auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, ARGMAX, LAY>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the attributes are set once per instantiation and device (and again for
+  // a larger shared-memory size): a launch then costs no attribute calls
+  static std::atomic<uint64_t> set_for{0};           // (device + 1) << 32 | bytes of the last setting
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
+  const uint64_t cur = set_for.load(std::memory_order_relaxed);
+  if ((cur >> 32) != (uint64_t)(dev + 1) || (cur & 0xFFFFFFFFu) < smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    set_for.store(((uint64_t)(dev + 1) << 32) | (uint64_t)smem, std::memory_order_relaxed);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(LAY == 1 ? kThreadsRing : kThreads);
@@ -1262,7 +1273,19 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, kern, tc, ts, tb, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tc, ts, tb, p);
+  if (e == cudaErrorInvalidValue) {
+    // the attributes may have been lost with the context (a device reset):
+    // set them again and retry once
+    (void)cudaGetLastError();
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    set_for.store(((uint64_t)(dev + 1) << 32) | (uint64_t)smem, std::memory_order_relaxed);
+    e = cudaLaunchKernelEx(&cfg, kern, tc, ts, tb, p);
+  }
+  return e;
 }
 
 // Clusters of ks CTAs of one kernel variant that fit on the GPU at once.
@@ -1360,12 +1383,55 @@ bool have_variant(int fmt, int uw, int mt, int gpm, bool argmax) {
 
 }  // namespace
 
-cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
-                           float *y, int M, int64_t N, int64_t K, int bits, int group, cudaStream_t s) {
-  if (M < 1 || M > 8) return cudaErrorNotSupported;
-  TcParams p{};
-  int uw = 0, grid = 0;
-  size_t smem = 0;
+namespace {
+
+// Plans and tensor maps of recent calls, keyed by the weight pointers, the
+// shape, the format and the device: a repeated call (a decode loop issuing
+// the same projections every token) skips planning, the cluster occupancy
+// query and the three tensor-map encodings.  A tensor map holds addresses,
+// sizes and strides only, so the weights' contents may change freely.
+struct PlanKey {
+  const void *codes, *scales, *biases;
+  int64_t N, K;
+  int M, bits, group, argmax, dev;
+  bool operator==(const PlanKey &o) const {
+    return codes == o.codes && scales == o.scales && biases == o.biases && N == o.N && K == o.K && M == o.M &&
+           bits == o.bits && group == o.group && argmax == o.argmax && dev == o.dev;
+  }
+};
+struct PlanVal {
+  bool ok;                       // false: the kernel does not take this call
+  TcParams p;
+  int uw, grid;
+  size_t smem;
+  CUtensorMap tc, ts, tb;
+};
+constexpr int kPlanCache = 64;
+std::mutex g_plan_mutex;
+PlanKey g_plan_keys[kPlanCache];
+PlanVal g_plan_vals[kPlanCache];
+int g_plan_count = 0, g_plan_next = 0;
+
+bool plan_lookup(const PlanKey &k, PlanVal &v) {
+  std::lock_guard<std::mutex> lock(g_plan_mutex);
+  for (int i = 0; i < g_plan_count; i++)
+    if (g_plan_keys[i] == k) {
+      v = g_plan_vals[i];
+      return true;
+    }
+  return false;
+}
+void plan_store(const PlanKey &k, const PlanVal &v) {
+  std::lock_guard<std::mutex> lock(g_plan_mutex);
+  g_plan_keys[g_plan_next] = k;
+  g_plan_vals[g_plan_next] = v;
+  g_plan_next = (g_plan_next + 1) % kPlanCache;
+  if (g_plan_count < kPlanCache) g_plan_count++;
+}
+
+// The plan of a decode product on the tensor-core kernel (false: not taken).
+bool plan_gemv_tc(int M, int64_t N, int64_t K, int bits, int group, TcParams &p, int &uw, int &grid,
+                  size_t &smem) {
   bool planned = false;
   // the K split is measured faster for 8-bit codes with 5 to 8 tokens and
   // for binary codes; otherwise it is the fallback of the resident-slab plan
@@ -1389,31 +1455,55 @@ cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t
       planned = true;
     }
   }
-  if (!planned && (M >= 2 && !split_first)) return cudaErrorNotSupported;
-  if (!planned && !plan_tc(bits, M, N, K, group, false, p, uw, grid, smem)) return cudaErrorNotSupported;
-  CUtensorMap tc, ts, tb;
-  if (!encode_maps(p, codes, scales, biases, tc, ts, tb)) return cudaErrorNotSupported;
+  if (!planned && (M >= 2 && !split_first)) return false;
+  if (!planned && !plan_tc(bits, M, N, K, group, false, p, uw, grid, smem)) return false;
+  return true;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_tc(const float *x, const uint32_t *codes, const uint16_t *scales, const uint16_t *biases,
+                           float *y, int M, int64_t N, int64_t K, int bits, int group, cudaStream_t s) {
+  if (M < 1 || M > 8) return cudaErrorNotSupported;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
+  const PlanKey key{codes, scales, biases, N, K, M, bits, group, 0, dev};
+  PlanVal v;
+  if (!plan_lookup(key, v)) {
+    v = PlanVal{};
+    v.ok = plan_gemv_tc(M, N, K, bits, group, v.p, v.uw, v.grid, v.smem) &&
+           encode_maps(v.p, codes, scales, biases, v.tc, v.ts, v.tb);
+    plan_store(key, v);
+  }
+  if (!v.ok) return cudaErrorNotSupported;
+  TcParams p = v.p;
   p.x = x;
   p.y = y;
   p.test_wait_ns = g_tc_test_wait_ns.exchange(0);
-  if (p.ks > 1) return launch_tc_split(bits, uw, M > 4 ? 2 : 1, p.gpm, tc, ts, tb, p, grid, smem, s);
-  return launch_tc<false>(bits, uw, M > 4 ? 2 : 1, p.gpm, tc, ts, tb, p, grid, smem, s);
+  if (p.ks > 1) return launch_tc_split(bits, v.uw, M > 4 ? 2 : 1, p.gpm, v.tc, v.ts, v.tb, p, v.grid, v.smem, s);
+  return launch_tc<false>(bits, v.uw, M > 4 ? 2 : 1, p.gpm, v.tc, v.ts, v.tb, p, v.grid, v.smem, s);
 }
 
 cudaError_t launch_gemv_tc_argmax(const float *x, const uint32_t *codes, const uint16_t *scales,
                                   const uint16_t *biases, int64_t N, int64_t K, int bits, int group,
                                   const ArgmaxWork &w, cudaStream_t s) {
-  TcParams p{};
-  int uw = 0, grid = 0;
-  size_t smem = 0;
-  if (!plan_tc(bits, 1, N, K, group, true, p, uw, grid, smem) || grid > kArgmaxMaxCtas) return cudaErrorNotSupported;
-  CUtensorMap tc, ts, tb;
-  if (!encode_maps(p, codes, scales, biases, tc, ts, tb)) return cudaErrorNotSupported;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorNotSupported;
+  const PlanKey key{codes, scales, biases, N, K, 1, bits, group, 1, dev};
+  PlanVal v;
+  if (!plan_lookup(key, v)) {
+    v = PlanVal{};
+    v.ok = plan_tc(bits, 1, N, K, group, true, v.p, v.uw, v.grid, v.smem) && v.grid <= kArgmaxMaxCtas &&
+           encode_maps(v.p, codes, scales, biases, v.tc, v.ts, v.tb);
+    plan_store(key, v);
+  }
+  if (!v.ok) return cudaErrorNotSupported;
+  TcParams p = v.p;
   p.x = x;
   p.y = nullptr;
   p.am = w;
   p.test_wait_ns = g_tc_test_wait_ns.exchange(0);
-  return launch_tc<true>(bits, uw, 1, p.gpm, tc, ts, tb, p, grid, smem, s);
+  return launch_tc<true>(bits, v.uw, 1, p.gpm, v.tc, v.ts, v.tb, p, v.grid, v.smem, s);
 }
 
 void set_tc_test_wait(unsigned long long limit_ns) { g_tc_test_wait_ns.store(limit_ns); }
