@@ -132,6 +132,7 @@ struct TcParams {
   int nact0, nact1;          // active B lanes per MMA in column blocks 0 and 1
   int pstr0, pstr1;          // bytes per MMA pair of B in column blocks 0 and 1 (16 * nact + 16)
   int off_b, off_xs, off_red, off_zero, off_bar, off_am, off_tw;
+  int gs;                    // INT4 group 64, one token, resident slab: k-loop in whole group sets (1) or k-steps (0)
   ArgmaxWork am;
   // K split over a cluster of ks CTAs (wide only; 1: no split).  Rank r of a
   // cluster takes the slice of row_words words (NG groups) starting at word
@@ -250,10 +251,15 @@ __device__ __forceinline__ void b_lane(int gpm, int m, int t, int tau, int &cb, 
 
 // ---------------------------------------------------------------- kernel
 
-// Not wide: with W working warps (W = min(16, steps)), warp w takes the
-// k-steps [run(w), run(w + 1)) of the slab's tiles, in (tile, k-step) order;
-// every run is non-empty.
-__host__ __device__ __forceinline__ int run_begin(int w, int W, int total) { return w * total / W; }
+// Not wide: with W working warps (W = min(16, units)), warp w takes the
+// work units [run(w), run(w + 1)) of the slab's tiles, in (tile, unit) order;
+// every run is non-empty.  The first total % W warps take one unit more, so
+// that the four warp schedulers of an SM (warp w on scheduler w % 4) get
+// equal shares to within one unit: the loop is bound by each scheduler's issue.
+__host__ __device__ __forceinline__ int run_begin(int w, int W, int total) {
+  const int q = total / W, r = total - q * W;
+  return w * q + (w < r ? w : r);
+}
 
 // LAY: 0 resident slab (one-token kernels; the others also take a ring at
 // run time), 1 ring (one-token kernels for long slabs, whose shared memory
@@ -318,9 +324,12 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
     }
     mbar_init(bars + 8 * (2 * S) + 8, 1);      // test hook: initialised, never arrived on
     *abort_flag = 0;
-    *reinterpret_cast<uint4 *>(smem + p.off_zero) = make_uint4(0u, 0u, 0u, 0u);   // B of inactive lanes
     fence_mbar_init();
   }
+  // B of inactive lanes: 16 zero bytes, or 1 KB in the group-set loop (which
+  // reads them at the immediate offsets of an active lane's eight fragments)
+  if (threadIdx.x < (p.gs ? 64 : 1))
+    reinterpret_cast<uint4 *>(smem + p.off_zero)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   pdl_launch_dependents();
 
@@ -375,7 +384,13 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
   const int nthreads = nwarps * 32;
   const int ct = cw * 32 + lane;
   const int g = lane >> 2, t = lane & 3;
-  const int total_steps = ntiles * spt;
+  // INT4 group 64 with one token (the MLP shapes): the resident-slab loop
+  // takes whole group sets (the lane quad's four groups, two k-steps) as its
+  // work units, with addresses advanced by constants
+  constexpr bool GS_T = FMT == 4 && GPM == 4 && MT == 1 && UW == 4 && LAY == 0;
+  const bool gs = GS_T && p.gs != 0;
+  const int upt = gs ? (spt >> 1) : spt;                   // work units per tile
+  const int total_steps = ntiles * upt;
   const int W = total_steps < 16 ? total_steps : 16;    // not wide: working warps
   // not wide: wait for the slab before the dependent-launch wait (its copies
   // were issued at the start; the wait overlaps the previous kernel's tail)
@@ -718,7 +733,69 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
 
   uint4 bf[MT][NQ];
   float d[2][MT][4];
-  if (!wide) {
+  if (gs) {
+    if constexpr (GS_T) {
+      // Group-set units.  Unit j of a tile is group set j: lane t takes group
+      // 4j + t, whose 8 code words of a row are the 16-byte chunks 2t and
+      // 2t + 1 of 128-byte column j (before the swizzle; the two differ in
+      // address bit 4 after it), and whose B fragments are the 8 MMA pairs
+      // from 8j on (144 bytes apart: 8 active lanes plus the padding).
+      // Inactive B lanes read a 1 KB zero block at the same offsets.
+      if (ok && se > sb) {
+        int tile = sb / upt;
+        int j = sb - tile * upt;
+        bool first = j == 0;                                   // this warp took the tile's first unit
+        const int bstep = bstr[0] * 8;                         // 1152, or 0 for an inactive lane
+        int oa0 = 0, ob0 = 0;
+        auto tile_rows = [&](int tl) {
+          set_rows(0, min(tl * kTileRows + g, rows - 1), min(tl * kTileRows + g + 8, rows - 1));
+          oa0 = ca + (((2 * t) ^ swa) << 4);
+          ob0 = cb8 + (((2 * t) ^ swb) << 4);
+        };
+        tile_rows(tile);
+        const uint8_t *bp = smem + bofs0[0] + j * bstep;
+        auto mma_words = [&](const uint4 &wa4, const uint4 &wb4, const uint8_t *b8, float (&e)[2][MT][4]) {
+          const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w}, wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
+#pragma unroll
+          for (int u = 0; u < 4; u++) {
+            const uint4 b = lds128(b8 + u * 144);
+            const uint32_t w = wa[u], v = wb[u], w8 = w >> 8, v8 = v >> 8;
+            if (u == 0) {
+              mma_f16_z(e[0][0], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
+              mma_f16_z(e[1][0], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
+            } else {
+              mma_f16(e[0][0], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
+              mma_f16(e[1][0], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
+            }
+          }
+        };
+        for (int s = sb; s < se; s++) {
+          const int cofs = j << 10;                            // column j (8-row boxes: 1 KB columns)
+          float e1[2][MT][4];
+          mma_words(lds128(smem + oa0 + cofs), lds128(smem + ob0 + cofs), bp, d);
+          mma_words(lds128(smem + (oa0 ^ 16) + cofs), lds128(smem + (ob0 ^ 16) + cofs), bp + 4 * 144, e1);
+#pragma unroll
+          for (int h = 0; h < 2; h++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) d[h][0][i] += e1[h][0][i];
+          step_epi(4 * j + t, true, d);
+          bp += bstep;
+          j++;
+          if (j == upt || s + 1 == se) {
+            flush(cw + tile);                                  // (warp, tile) -> warp + tile is one-to-one
+            if (lane == 0 && first) tw[2 * tile] = cw;
+            if (lane == 0 && j == upt) tw[2 * tile + 1] = cw;
+            if (s + 1 == se) break;
+            tile++;
+            j = 0;
+            first = true;
+            bp = smem + bofs0[0];
+            tile_rows(tile);
+          }
+        }
+      }
+    }
+  } else if (!wide) {
     if (ok && se > sb) {
       int tile = sb / spt;
       int pst = (sb - tile * spt) * UW;                        // lane word position in the tile row
@@ -969,6 +1046,10 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   size_t bbytes = (size_t)nj2 * (pstr0 + pstr1);
   const size_t xsbytes = (size_t)M * NG * 16;              // {2^-24 sum x', f1, f2} per (token, group)
   const size_t misc = 16 + 256 + kAmScratch + 16 + 1024;  // zero block, tile table, argmax scratch, abort, alignment
+  // INT4 group 64 with one token: the slab loop in group sets, whose inactive
+  // B lanes read a 1 KB zero block (1008 bytes more than the 16 above)
+  const bool gs_fmt = fmt == 4 && gpm == 4 && mt == 1 && wpg == 8;
+  const size_t gs_extra = gs_fmt ? 1008 : 0;
 
   // rows per CTA: the 8-row blocks of N split evenly over one CTA per SM (so
   // that no SM holds two CTAs of one product); a slab is copied as 8-row
@@ -988,14 +1069,14 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
     // resident slab (up to 256 rows): warps take runs of k-steps
     if (R <= 256) {
       const size_t slab = align1k((size_t)R * row_bytes + (size_t)ncoef * R * NG * 2);
-      const size_t rest = xsbytes + (size_t)(15 + ntiles) * M * kTileRows * 4 + misc + 16;
+      const size_t rest = xsbytes + (size_t)(15 + ntiles) * M * kTileRows * 4 + misc + gs_extra + 16;
       if (slab + bbytes + rest > (size_t)kSmemPair && slab + (size_t)nj2 * (nact0 + nact1) * 16 + rest <= (size_t)kSmemPair) {
         pstr0 = nact0 * 16;
         pstr1 = nact1 * 16;
         bbytes = (size_t)nj2 * (pstr0 + pstr1);
       }
       // partial sums: one slot per (warp, tile) of the runs, warp + tile
-      const size_t sm = slab + bbytes + xsbytes + (size_t)(15 + ntiles) * M * kTileRows * 4 + misc + 16;
+      const size_t sm = slab + bbytes + xsbytes + (size_t)(15 + ntiles) * M * kTileRows * 4 + misc + gs_extra + 16;
       if (sm <= (size_t)kSmemMax) {
         const double cost = (double)((ntiles * spt + 15) / 16) * step_cost;
         if (cost < best_cost) {
@@ -1063,6 +1144,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   p.nact1 = nact1;
   p.pstr0 = pstr0;
   p.pstr1 = pstr1;
+  p.gs = gs_fmt && !best_wide && best_uw == 4 && pstr0 == 144 && best_spt % 2 == 0 ? 1 : 0;
   if (best_wide) grid = sms < (N + 7) / 8 ? sms : (int)((N + 7) / 8);
   else grid = grid_nw;
   const int nt_red = best_wide ? (int)((N + grid - 1) / grid + kTileRows - 1) / kTileRows : ntiles;
@@ -1074,7 +1156,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   p.off_red = (int)off;
   off += (best_wide ? (size_t)nt_red * best_nks : (size_t)(15 + ntiles)) * M * kTileRows * 4;
   p.off_zero = (int)off;
-  off += 16;
+  off += p.gs ? 1024 : 16;
   p.off_tw = (int)off;
   off += 8 * 32;
   p.off_bar = (int)off;
@@ -1178,6 +1260,7 @@ bool plan_tc_split(int fmt, int M, int64_t N, int64_t K, int group, int ks, int 
   p.nact1 = nact1;
   p.pstr0 = pstr0;
   p.pstr1 = pstr1;
+  p.gs = 0;
   size_t off = (size_t)S * stage;
   p.off_b = (int)off;
   off += bbytes;
