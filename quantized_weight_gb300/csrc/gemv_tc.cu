@@ -400,137 +400,9 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
   // stop at an abort, so the CTA never exits with a copy in flight)
   bool ok = true;
   if (!wide) ok = __all_sync(0xffffffffu, wait_bounded(bars, 0, ctl, kWaitLimitNs, warp != 0));
-  {
-    // one MMA on zeros while the previous kernel finishes: the first MMA of a
-    // CTA is slow, and this moves its cost off the dependent path (measured
-    // 60-70 ns less per chained product)
-    float dz[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    mma_f16(dz, 0u, 0u, 0u, 0u, 0u, 0u);
-    asm volatile("" ::"f"(dz[0]), "f"(dz[1]), "f"(dz[2]), "f"(dz[3]));
-  }
-  pdl_wait();                                                  // x is written by the previous kernel
 
-  // ---------------------------------------------- activation preparation
-  // One pass, a thread per (token, code word), 16 floats of x per thread
-  // per round: per group g of token m the scale 2^S (largest |x| of the group
-  // in [2^14, 2^15)); x' = x * 2^S split into binary16 hi + lo and stored as
-  // B fragments; per (m, g) the constants {2^-24 sum x', f1, f2} with
-  // f1 * f2 = 2^(24 - S).  A warp's 32 words lie in one token (row_words is a
-  // multiple of 32) and a group's words in wpg adjacent lanes.
-  {
-    constexpr int NB = F::WPK >= 16 ? 1 : 16 / F::WPK;        // words per thread per round
-    const int total_words = M * row_words;
-    float4 *xgw = reinterpret_cast<float4 *>(smem + p.off_xs);
-    for (int base0 = cw * 32; base0 < total_words; base0 += NB * nthreads) {
-      float xv[NB][F::WPK];
-#pragma unroll
-      for (int b = 0; b < NB; b++) {
-        // word u of the (token, slice word) sequence; a warp's 32 words lie in
-        // one token, whose slice starts at word crank * row_words of x's row
-        const int ub = base0 + b * nthreads;
-        int64_t xo = 0;                                            // float offset of word ub + lane
-        if (ub < total_words) {
-          xo = (int64_t)(ub + lane) * F::WPK;
-          if constexpr (SPLIT) {
-            const int mu = ub / row_words;
-            xo += (int64_t)mu * (p.K - row_words * F::WPK) + (int64_t)crank * row_words * F::WPK;
-          }
-        }
-        const float4 *src = reinterpret_cast<const float4 *>(p.x + xo);
-#pragma unroll
-        for (int i = 0; i < F::WPK / 4; i++) {
-          const float4 v = __ldg(src + i);
-          xv[b][4 * i] = v.x;
-          xv[b][4 * i + 1] = v.y;
-          xv[b][4 * i + 2] = v.z;
-          xv[b][4 * i + 3] = v.w;
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < NB; b++) {
-        const int ubase = base0 + b * nthreads;
-        if (ubase >= total_words) break;                       // warp-uniform
-        const int u = ubase + lane;
-        const bool valid = u < total_words;
-        const int m = ubase / row_words;
-        const int wd = u - m * row_words;
-        // the group's largest |x| and its sum, reduced in the same shuffle
-        // rounds; the sum of x' = 2^S x is the sum of x times 2^S (scaling by
-        // a power of two commutes with rounding away from over- and underflow)
-        uint32_t mx = 0u;
-        float rsum = 0.0f;
-#pragma unroll
-        for (int e = 0; e < F::WPK; e++) {
-          mx = max(mx, absbits(xv[b][e]));
-          rsum += xv[b][e];
-        }
-        if (!valid) mx = 0u, rsum = 0.0f;
-        for (int o = 1; o < wpg; o <<= 1) {
-          const uint32_t om = __shfl_xor_sync(0xffffffffu, mx, o);
-          const float os = __shfl_xor_sync(0xffffffffu, rsum, o);
-          mx = max(mx, om);
-          rsum += os;
-        }
-        const int Sx = scale_exp(mx);
-        const float sc = pow2f(Sx);
-#pragma unroll
-        for (int e = 0; e < F::WPK; e++) xv[b][e] *= sc;
-        const float wsum = rsum * sc;
-        if (!valid) continue;
-        const int grp = wd >> lg_wpg, wig = wd & (wpg - 1);
-        if (wig == 0) {
-          const int ex = 24 - Sx, e1 = ex > 127 ? 127 : ex;
-          xgw[m * NG + grp] = make_float4(wsum * 5.9604644775390625e-08f, pow2f(e1), pow2f(ex - e1), 0.0f);
-        }
-        // this word's lane and position in the MMA sequence
-        const int gq = grp >> LG_GPM, gsel = grp & (GPM - 1);
-        const int lt = (gsel << LG_LPG) + (wig >> lg_wl);
-        const int pos = (gq << lg_wl) + (wig & (wl - 1));
-#pragma unroll
-        for (int tau = 0; tau < 2; tau++) {
-          int cb, ai;
-          b_lane(GPM, m, lt, tau, cb, ai);
-          const int pstr = cb ? pstr1 : pstr0;
-          uint8_t *bbase = smem + p.off_b + cb * nj2 * pstr0;
-          if constexpr (FMT == 4) {
-            // MMA pair (P, Q) of this word: P (e0, e4 | e1, e5), Q (e2, e6 | e3, e7)
-            uint32_t h[4], l[4];
-            split_pair(xv[b][0], xv[b][4], h[0], l[0]);
-            split_pair(xv[b][1] * 0.0625f, xv[b][5] * 0.0625f, h[1], l[1]);
-            split_pair(xv[b][2], xv[b][6], h[2], l[2]);
-            split_pair(xv[b][3] * 0.0625f, xv[b][7] * 0.0625f, h[3], l[3]);
-            const uint32_t *v = tau ? l : h;
-            *reinterpret_cast<uint4 *>(bbase + pos * pstr + ai * 16) = make_uint4(v[0], v[1], v[2], v[3]);
-          } else if constexpr (FMT == 8) {
-            uint32_t h[2], l[2];
-            split_pair(xv[b][0], xv[b][1], h[0], l[0]);
-            split_pair(xv[b][2], xv[b][3], h[1], l[1]);
-            const uint32_t *v = tau ? l : h;
-            *reinterpret_cast<uint2 *>(bbase + (pos >> 1) * pstr + ai * 16 + 8 * (pos & 1)) = make_uint2(v[0], v[1]);
-          } else {
-            // MMA j of the word: (e_2j, e_16+2j | e_2j+1, e_17+2j), element e of a
-            // half at bit position e (e <= 10) or e - 11, so divided by that power
-#pragma unroll
-            for (int jp = 0; jp < 4; jp++) {
-              uint32_t v[4];
-#pragma unroll
-              for (int q = 0; q < 4; q++) {
-                const int i = 4 * jp + q;                  // register index 0..15 (= 2j or 2j + 1)
-                const float f = 1.0f / (float)(1 << (i <= 10 ? i : i - 11));
-                uint32_t hh, ll;
-                split_pair(xv[b][i] * f, xv[b][16 + i] * f, hh, ll);
-                v[q] = tau ? ll : hh;
-              }
-              *reinterpret_cast<uint4 *>(bbase + (pos * 4 + jp) * pstr + ai * 16) = make_uint4(v[0], v[1], v[2], v[3]);
-            }
-          }
-        }
-      }
-    }
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-
-  // ---------------------------------------------------------- products
+  // ------------------------------------------- products: setup and helpers
+  // (none of it depends on x, so it runs before the dependent-launch wait)
   // B fragments of this lane: byte offset and stride per MMA pair (inactive
   // lanes read 16 zero bytes)
   int bofs0[MT], bstr[MT], tokofs[MT], tokv[MT];
@@ -731,6 +603,164 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
     }
   };
 
+
+  // Group-set loop (INT4 group 64, one token): per-lane state and the MMAs of
+  // four code words of rows g and g + 8 (two k-steps make a group set)
+  const int bstep = bstr[0] * 8;                 // B bytes per group set: 1152, or 0 for an inactive lane
+  int oa0 = 0, ob0 = 0;                          // chunk 2t of rows g and g + 8 in column 0 (after the swizzle)
+  auto tile_rows = [&](int tl) {
+    set_rows(0, min(tl * kTileRows + g, rows - 1), min(tl * kTileRows + g + 8, rows - 1));
+    oa0 = ca + (((2 * t) ^ swa) << 4);
+    ob0 = cb8 + (((2 * t) ^ swb) << 4);
+  };
+  auto mma_words = [&](const uint4 &wa4, const uint4 &wb4, const uint8_t *b8, float (&e)[2][MT][4]) {
+    const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w}, wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const uint4 b = lds128(b8 + u * 144);
+      const uint32_t w = wa[u], v = wb[u], w8 = w >> 8, v8 = v >> 8;
+      if (u == 0) {
+        mma_f16_z(e[0][0], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
+        mma_f16_z(e[1][0], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
+      } else {
+        mma_f16(e[0][0], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
+        mma_f16(e[1][0], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
+      }
+    }
+  };
+
+  {
+    // one MMA on zeros while the previous kernel finishes: the first MMA of a
+    // CTA is slow, and this moves its cost off the dependent path (measured
+    // 60-70 ns less per chained product)
+    float dz[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    mma_f16(dz, 0u, 0u, 0u, 0u, 0u, 0u);
+    asm volatile("" ::"f"(dz[0]), "f"(dz[1]), "f"(dz[2]), "f"(dz[3]));
+  }
+  pdl_wait();                                                  // x is written by the previous kernel
+
+  // ---------------------------------------------- activation preparation
+  // One pass, a thread per (token, code word), 16 floats of x per thread
+  // per round: per group g of token m the scale 2^S (largest |x| of the group
+  // in [2^14, 2^15)); x' = x * 2^S split into binary16 hi + lo and stored as
+  // B fragments; per (m, g) the constants {2^-24 sum x', f1, f2} with
+  // f1 * f2 = 2^(24 - S).  A warp's 32 words lie in one token (row_words is a
+  // multiple of 32) and a group's words in wpg adjacent lanes.
+  {
+    constexpr int NB = F::WPK >= 16 ? 1 : 16 / F::WPK;        // words per thread per round
+    const int total_words = M * row_words;
+    float4 *xgw = reinterpret_cast<float4 *>(smem + p.off_xs);
+    for (int base0 = cw * 32; base0 < total_words; base0 += NB * nthreads) {
+      float xv[NB][F::WPK];
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        // word u of the (token, slice word) sequence; a warp's 32 words lie in
+        // one token, whose slice starts at word crank * row_words of x's row
+        const int ub = base0 + b * nthreads;
+        int64_t xo = 0;                                            // float offset of word ub + lane
+        if (ub < total_words) {
+          xo = (int64_t)(ub + lane) * F::WPK;
+          if constexpr (SPLIT) {
+            const int mu = ub / row_words;
+            xo += (int64_t)mu * (p.K - row_words * F::WPK) + (int64_t)crank * row_words * F::WPK;
+          }
+        }
+        const float4 *src = reinterpret_cast<const float4 *>(p.x + xo);
+#pragma unroll
+        for (int i = 0; i < F::WPK / 4; i++) {
+          const float4 v = __ldg(src + i);
+          xv[b][4 * i] = v.x;
+          xv[b][4 * i + 1] = v.y;
+          xv[b][4 * i + 2] = v.z;
+          xv[b][4 * i + 3] = v.w;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; b++) {
+        const int ubase = base0 + b * nthreads;
+        if (ubase >= total_words) break;                       // warp-uniform
+        const int u = ubase + lane;
+        const bool valid = u < total_words;
+        const int m = ubase / row_words;
+        const int wd = u - m * row_words;
+        // the group's largest |x| and its sum, reduced in the same shuffle
+        // rounds; the sum of x' = 2^S x is the sum of x times 2^S (scaling by
+        // a power of two commutes with rounding away from over- and underflow)
+        uint32_t mx = 0u;
+        float rsum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < F::WPK; e++) {
+          mx = max(mx, absbits(xv[b][e]));
+          rsum += xv[b][e];
+        }
+        if (!valid) mx = 0u, rsum = 0.0f;
+        for (int o = 1; o < wpg; o <<= 1) {
+          const uint32_t om = __shfl_xor_sync(0xffffffffu, mx, o);
+          const float os = __shfl_xor_sync(0xffffffffu, rsum, o);
+          mx = max(mx, om);
+          rsum += os;
+        }
+        const int Sx = scale_exp(mx);
+        const float sc = pow2f(Sx);
+#pragma unroll
+        for (int e = 0; e < F::WPK; e++) xv[b][e] *= sc;
+        const float wsum = rsum * sc;
+        if (!valid) continue;
+        const int grp = wd >> lg_wpg, wig = wd & (wpg - 1);
+        if (wig == 0) {
+          const int ex = 24 - Sx, e1 = ex > 127 ? 127 : ex;
+          xgw[m * NG + grp] = make_float4(wsum * 5.9604644775390625e-08f, pow2f(e1), pow2f(ex - e1), 0.0f);
+        }
+        // this word's lane and position in the MMA sequence
+        const int gq = grp >> LG_GPM, gsel = grp & (GPM - 1);
+        const int lt = (gsel << LG_LPG) + (wig >> lg_wl);
+        const int pos = (gq << lg_wl) + (wig & (wl - 1));
+        // the hi terms go to the B lane of term 0, the lo terms to that of term 1
+        uint8_t *bb[2];
+        int ps[2];
+#pragma unroll
+        for (int tau = 0; tau < 2; tau++) {
+          int cb, ai;
+          b_lane(GPM, m, lt, tau, cb, ai);
+          ps[tau] = cb ? pstr1 : pstr0;
+          bb[tau] = smem + p.off_b + cb * nj2 * pstr0 + ai * 16;
+        }
+        if constexpr (FMT == 4) {
+          // MMA pair (P, Q) of this word: P (e0, e4 | e1, e5), Q (e2, e6 | e3, e7)
+          uint32_t h[4], l[4];
+          split_pair(xv[b][0], xv[b][4], h[0], l[0]);
+          split_pair(xv[b][1] * 0.0625f, xv[b][5] * 0.0625f, h[1], l[1]);
+          split_pair(xv[b][2], xv[b][6], h[2], l[2]);
+          split_pair(xv[b][3] * 0.0625f, xv[b][7] * 0.0625f, h[3], l[3]);
+          *reinterpret_cast<uint4 *>(bb[0] + pos * ps[0]) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4 *>(bb[1] + pos * ps[1]) = make_uint4(l[0], l[1], l[2], l[3]);
+        } else if constexpr (FMT == 8) {
+          uint32_t h[2], l[2];
+          split_pair(xv[b][0], xv[b][1], h[0], l[0]);
+          split_pair(xv[b][2], xv[b][3], h[1], l[1]);
+          *reinterpret_cast<uint2 *>(bb[0] + (pos >> 1) * ps[0] + 8 * (pos & 1)) = make_uint2(h[0], h[1]);
+          *reinterpret_cast<uint2 *>(bb[1] + (pos >> 1) * ps[1] + 8 * (pos & 1)) = make_uint2(l[0], l[1]);
+        } else {
+          // MMA j of the word: (e_2j, e_16+2j | e_2j+1, e_17+2j), element e of a
+          // half at bit position e (e <= 10) or e - 11, so divided by that power
+#pragma unroll
+          for (int jp = 0; jp < 4; jp++) {
+            uint32_t hh[4], ll[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+              const int i = 4 * jp + q;                    // register index 0..15 (= 2j or 2j + 1)
+              const float f = 1.0f / (float)(1 << (i <= 10 ? i : i - 11));
+              split_pair(xv[b][i] * f, xv[b][16 + i] * f, hh[q], ll[q]);
+            }
+            *reinterpret_cast<uint4 *>(bb[0] + (pos * 4 + jp) * ps[0]) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+            *reinterpret_cast<uint4 *>(bb[1] + (pos * 4 + jp) * ps[1]) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+          }
+        }
+      }
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+
   uint4 bf[MT][NQ];
   float d[2][MT][4];
   if (gs) {
@@ -745,30 +775,8 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
         int tile = sb / upt;
         int j = sb - tile * upt;
         bool first = j == 0;                                   // this warp took the tile's first unit
-        const int bstep = bstr[0] * 8;                         // 1152, or 0 for an inactive lane
-        int oa0 = 0, ob0 = 0;
-        auto tile_rows = [&](int tl) {
-          set_rows(0, min(tl * kTileRows + g, rows - 1), min(tl * kTileRows + g + 8, rows - 1));
-          oa0 = ca + (((2 * t) ^ swa) << 4);
-          ob0 = cb8 + (((2 * t) ^ swb) << 4);
-        };
         tile_rows(tile);
         const uint8_t *bp = smem + bofs0[0] + j * bstep;
-        auto mma_words = [&](const uint4 &wa4, const uint4 &wb4, const uint8_t *b8, float (&e)[2][MT][4]) {
-          const uint32_t wa[4] = {wa4.x, wa4.y, wa4.z, wa4.w}, wb[4] = {wb4.x, wb4.y, wb4.z, wb4.w};
-#pragma unroll
-          for (int u = 0; u < 4; u++) {
-            const uint4 b = lds128(b8 + u * 144);
-            const uint32_t w = wa[u], v = wb[u], w8 = w >> 8, v8 = v >> 8;
-            if (u == 0) {
-              mma_f16_z(e[0][0], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
-              mma_f16_z(e[1][0], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
-            } else {
-              mma_f16(e[0][0], w & 0x000F000Fu, v & 0x000F000Fu, w & 0x00F000F0u, v & 0x00F000F0u, b.x, b.y);
-              mma_f16(e[1][0], w8 & 0x000F000Fu, v8 & 0x000F000Fu, w8 & 0x00F000F0u, v8 & 0x00F000F0u, b.z, b.w);
-            }
-          }
-        };
         for (int s = sb; s < se; s++) {
           const int cofs = j << 10;                            // column j (8-row boxes: 1 KB columns)
           float e1[2][MT][4];
