@@ -51,8 +51,8 @@
 // so they are issued before the programmatic-dependent-launch wait.  The 16
 // warps then take runs of (16-row tile, k-step) work.  Longer slabs (a
 // vocabulary head) stream through a ring of 16-row stages fed by a producer
-// warp, and their work units (tile, K slice) go round robin to 15 consumer
-// warps.  Partial sums land in per-(unit, row, token) shared-memory slots;
+// warp, and their work units (tile, K slice) go to 15 or 16 consumer warps,
+// each ring slot's own.  Partial sums land in per-(unit, row, token) shared-memory slots;
 // after a barrier one thread per output adds them in a fixed order: no
 // atomics, the same bits on every run.
 //
@@ -96,7 +96,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 512;              // 16 warps
-constexpr int kThreadsRing = 544;          // one-token ring: a producer warp and 16 consumer warps
+constexpr int kThreadsRing = 544;          // one-token ring and K split: a producer warp and 16 consumer warps
 constexpr int kTileRows = 16;              // rows per MMA tile and per stage
 constexpr int kSmemMax = 225 * 1024;
 constexpr int kSmemPair = 113 * 1024;      // at most this much shared memory: two CTAs per SM
@@ -267,7 +267,8 @@ __host__ __device__ __forceinline__ int run_begin(int w, int W, int total) {
 // cluster.  Separate instantiations keep each kernel's code to the
 // layout it runs (code a kernel carries but never runs measured 2 % slower).
 template <int FMT, int UW, int MT, int GPM, bool ARGMAX, int LAY>
-__global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 && LAY != 1 ? 2 : 1)
+__global__ void __launch_bounds__(LAY == 1 || (LAY == 2 && MT == 2) ? kThreadsRing : kThreads,
+                                  MT == 1 && LAY != 1 ? 2 : 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_biases, const TcParams p) {
   using F = Fmt<FMT>;
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bars = sbase + p.off_bar;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_bar + 8 * (2 * S));
-  const float4 *xgc = reinterpret_cast<const float4 *>(smem + p.off_xs);   // [M][NG] per-(token, group) constants
+  const float4 *xgc = reinterpret_cast<const float4 *>(smem + p.off_xs);   // [NG][M] per-(group, token) constants
   int *tw = reinterpret_cast<int *>(smem + p.off_tw);                       // not wide: [tile] first and last warp
   float *red = reinterpret_cast<float *>(smem + p.off_red);
   const WaitCtl ctl{abort_flag, &g_tc_status};
@@ -405,7 +406,14 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
   // (none of it depends on x, so it runs before the dependent-launch wait)
   // B fragments of this lane: byte offset and stride per MMA pair (inactive
   // lanes read 16 zero bytes)
-  int bofs0[MT], bstr[MT], tokofs[MT], tokv[MT];
+  // The tile rows of MMA rows g and g + 8.  A quarter-warp (lanes 8i .. 8i + 7)
+  // holds MMA rows 2i and 2i + 1; where each lane of a row reads its own
+  // 16-byte chunk (one or two groups per MMA: four chunks of a row per
+  // quarter-warp), rows 2i and 2i + 1 would read the same chunks after the
+  // 128-byte swizzle (2-way bank conflicts), so those MMA rows map to tile
+  // rows i and i + 4, whose swizzles differ in the chunk's bit 2.
+  const int gr = GPM == 4 ? g : ((g >> 1) | ((g & 1) << 2));
+  int bofs0[MT], bstr[MT], tokv[MT];
 #pragma unroll
   for (int cb = 0; cb < MT; cb++) {
     int active, ai;
@@ -423,7 +431,6 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
     bofs0[cb] = active ? p.off_b + cb * nj2 * pstr0 + ai * 16 : p.off_zero;
     // token whose results lane t holds in column block cb
     tokv[cb] = GPM == 4 ? 0 : GPM == 2 ? (t & 1) : min(4 * cb + t, M - 1);
-    tokofs[cb] = tokv[cb] * NG;
   }
   const int gsel_lane = t >> LG_LPG;                               // group of this lane within a group set
   const int wofs_lane = (t & (LPG - 1)) << lg_wl;                  // first word of this lane within its group
@@ -450,8 +457,8 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
       const bool writer = GPM == 4 ? t == 0 : GPM == 2 ? t < 2 : 4 * cb + t < M;
       if (writer) {
         float *dst = red + (slot * M + tokv[cb]) * kTileRows;
-        dst[g] = a0;
-        dst[g + 8] = a1;
+        dst[gr] = a0;
+        dst[gr + 8] = a1;
       }
       acc[cb][0] = acc[cb][1] = 0.0f;
     }
@@ -574,7 +581,7 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
     const uint16_t sah = lds16(smem + ka + kofs), sbh = lds16(smem + kb8 + kofs);
     float4 xc[MT];
 #pragma unroll
-    for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[tokofs[cb] + grp];
+    for (int cb = 0; cb < MT; cb++) xc[cb] = xgc[grp * M + tokv[cb]];
     float sa = h2f(sah), sbv = h2f(sbh);
     float ea = 0.0f, eb = 0.0f;
     if (withx) {
@@ -609,7 +616,7 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
   const int bstep = bstr[0] * 8;                 // B bytes per group set: 1152, or 0 for an inactive lane
   int oa0 = 0, ob0 = 0;                          // chunk 2t of rows g and g + 8 in column 0 (after the swizzle)
   auto tile_rows = [&](int tl) {
-    set_rows(0, min(tl * kTileRows + g, rows - 1), min(tl * kTileRows + g + 8, rows - 1));
+    set_rows(0, min(tl * kTileRows + gr, rows - 1), min(tl * kTileRows + gr + 8, rows - 1));
     oa0 = ca + (((2 * t) ^ swa) << 4);
     ob0 = cb8 + (((2 * t) ^ swb) << 4);
   };
@@ -709,7 +716,7 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
         const int grp = wd >> lg_wpg, wig = wd & (wpg - 1);
         if (wig == 0) {
           const int ex = 24 - Sx, e1 = ex > 127 ? 127 : ex;
-          xgw[m * NG + grp] = make_float4(wsum * 5.9604644775390625e-08f, pow2f(e1), pow2f(ex - e1), 0.0f);
+          xgw[grp * M + m] = make_float4(wsum * 5.9604644775390625e-08f, pow2f(e1), pow2f(ex - e1), 0.0f);
         }
         // this word's lane and position in the MMA sequence
         const int gq = grp >> LG_GPM, gsel = grp & (GPM - 1);
@@ -812,7 +819,7 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
       int grp = ((pst >> lg_wl) << LG_GPM) + gsel_lane;
       int word0 = grp * wpg + wofs_lane + wi;
       bool withx = wi == 0, zero = true;
-      set_rows(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
+      set_rows(0, min(tile * kTileRows + gr, rows - 1), min(tile * kTileRows + gr + 8, rows - 1));
       for (int s = sb; s < se; s++) {
         load_b(pst, bf);
         step_mma(word0, bf, d, zero, std::false_type{});
@@ -843,12 +850,12 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
           wi = 0;
           grp = gsel_lane;
           word0 = grp * wpg + wofs_lane;
-          set_rows(0, min(tile * kTileRows + g, rows - 1), min(tile * kTileRows + g + 8, rows - 1));
+          set_rows(0, min(tile * kTileRows + gr, rows - 1), min(tile * kTileRows + gr + 8, rows - 1));
         }
       }
     }
   } else {
-    // Each ring slot has its own nks consumer warps (S * nks <= 15), and a
+    // Each ring slot has its own nks consumer warps (S * nks <= 15 or 16), and a
     // warp takes its slot's tiles in order, so every wait is for the next
     // phase of its own slot: a phase parity can never be taken for another
     // lap (copies may land out of order)
@@ -857,7 +864,7 @@ __global__ void __launch_bounds__(LAY == 1 ? kThreadsRing : kThreads, MT == 1 &&
     for (int tile = slot, lap = 0; ok && cw < S * nks && tile < ntiles; tile += S, lap ^= 1) {
       const int u = tile * nks + kq;
       if (!__all_sync(0xffffffffu, wait_bounded(bars + 8 * slot, lap, ctl))) { ok = false; break; }
-      set_rows(slot * stage_bytes, g, g + 8);
+      set_rows(slot * stage_bytes, gr, gr + 8);
       int pst = kq * spu * UW;
       int wi = pst & (wl - 1);
       int grp = ((pst >> lg_wl) << LG_GPM) + gsel_lane;
@@ -1052,7 +1059,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
   // preparation) unless that costs a slab two CTAs per SM
   int pstr0 = nact0 * 16 + 16, pstr1 = nact1 ? nact1 * 16 + 16 : 0;
   size_t bbytes = (size_t)nj2 * (pstr0 + pstr1);
-  const size_t xsbytes = (size_t)M * NG * 16;              // {2^-24 sum x', f1, f2} per (token, group)
+  const size_t xsbytes = (size_t)M * NG * 16;              // {2^-24 sum x', f1, f2} per (group, token)
   const size_t misc = 16 + 256 + kAmScratch + 16 + 1024;  // zero block, tile table, argmax scratch, abort, alignment
   // INT4 group 64 with one token: the slab loop in group sets, whose inactive
   // B lanes read a 1 KB zero block (1008 bytes more than the 16 above)
@@ -1094,7 +1101,7 @@ bool plan_tc(int fmt, int M, int64_t N, int64_t K, int group, bool argmax, TcPar
       }
     }
     // ring of 16-row stages with a producer warp; each of the S slots has
-    // nks consumer warps (S * nks <= 15) taking its tiles in order, one K
+    // nks consumer warps (S * nks <= 16 with one token, else 15) taking its tiles in order, one K
     // slice each
     if (mt != 1) continue;
     const int rows_w = (int)((N + sms - 1) / sms);
@@ -1214,20 +1221,27 @@ bool plan_tc_split(int fmt, int M, int64_t N, int64_t K, int group, int ks, int 
     if (wl % c == 0 && have_variant(fmt, c, mt, gpm, false)) uw = c;
   if (!uw) return false;
   const int spt = npos / uw;
-  // each of the S ring slots has nks consumer warps (S * nks <= 15) taking
-  // its tiles in order; nks is chosen for the shortest longest warp
+  // each of the S ring slots has nks consumer warps (S * nks <= the
+  // consumer warps) taking its tiles in order; nks is chosen for the shortest
+  // longest warp.  Kernels for 5 to 8 tokens may run 16 consumer warps
+  // instead of 15 (a 17th warp) with one or two per slot, taken only where
+  // that shortens the longest warp: measured 25 % faster with 8-bit codes
+  // (a ring slot per tile), and 18 % slower for 4-bit codes with eight warps
+  // per slot (a two-stage ring)
   const size_t stage = align1k((size_t)kTileRows * row_bytes + (size_t)ncoef * kTileRows * NG * 2);
   const size_t cl = ((size_t)(ks - 1) * M * rmax * 4 + 4 * (size_t)(ks - 1) + 15) & ~(size_t)15;
-  int nks = 0, S = 0;
+  int nks = 0, S = 0, consumers = 15;
   size_t red = 0;
   long best = 0;
+  for (int cons = 15; cons <= (mt == 2 ? 16 : 15); cons++)
   for (int c = 1; c <= 8 && c <= spt && spt % c == 0; c <<= 1) {
-    const int sc = std::min(nt_w, 15 / c);
+    if (cons == 16 && c > 2) break;
+    const int sc = std::min(nt_w, cons / c);
     const size_t rc = (size_t)nt_w * c * M * kTileRows * 4;
     const size_t fixed = bbytes + xsbytes + rc + 16 + 256 + kAmScratch + cl + 1024 + 64;
     if (sc * stage + fixed + 16 * (size_t)sc > (size_t)kSmemMax) continue;
     const long cost = (long)((nt_w + sc - 1) / sc) * (spt / c);
-    if (!nks || cost < best) nks = c, S = sc, red = rc, best = cost;
+    if (!nks || cost < best) nks = c, S = sc, red = rc, best = cost, consumers = cons;
   }
   if (!nks) return false;
 
@@ -1262,7 +1276,7 @@ bool plan_tc_split(int fmt, int M, int64_t N, int64_t K, int group, int ks, int 
   p.coef_bytes = kTileRows * NG * 2;
   p.stage_bytes = (int)stage;
   p.warp0 = 1;
-  p.nwarps = 15;
+  p.nwarps = consumers;
   p.nj2 = nj2;
   p.nact0 = nact0;
   p.nact1 = nact1;
@@ -1349,7 +1363,7 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(LAY == 1 ? kThreadsRing : kThreads);
+  cfg.blockDim = dim3(32 * (p.warp0 + p.nwarps));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1381,12 +1395,12 @@ cudaError_t launch_tc_as(const CUtensorMap &tc, const CUtensorMap &ts, const CUt
 
 // Clusters of ks CTAs of one kernel variant that fit on the GPU at once.
 template <int FMT, int UW, int MT, int GPM>
-int max_clusters_as(int ks, size_t smem) {
+int max_clusters_as(int ks, size_t smem, int threads) {
   auto kern = gemv_tc_kernel<FMT, UW, MT, GPM, false, 2>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1450,9 +1464,9 @@ cudaError_t launch_tc_split(int fmt, int uw, int mt, int gpm, const CUtensorMap 
   return cudaErrorNotSupported;
 }
 
-int max_clusters(int fmt, int uw, int mt, int gpm, int ks, size_t smem) {
+int max_clusters(int fmt, int uw, int mt, int gpm, int ks, size_t smem, int threads) {
 #define QMM_TC(F_, U_, T_, G_) \
-  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_) return max_clusters_as<F_, U_, T_, G_>(ks, smem);
+  if (fmt == F_ && uw == U_ && mt == T_ && gpm == G_) return max_clusters_as<F_, U_, T_, G_>(ks, smem, threads);
   QMM_TC(4, 4, 1, 2) QMM_TC(4, 2, 1, 2)
   QMM_TC(8, 8, 1, 2) QMM_TC(8, 4, 1, 2)
   QMM_TC(4, 4, 1, 1) QMM_TC(4, 2, 1, 1) QMM_TC(4, 4, 2, 1) QMM_TC(4, 2, 2, 1)
@@ -1536,12 +1550,12 @@ bool plan_gemv_tc(int M, int64_t N, int64_t K, int bits, int group, TcParams &p,
       if (K / ks > 1024 && ks < 8) continue;
       int ncl = sms / ks;
       if (!plan_tc_split(bits, M, N, K, group, ks, ncl, p, uw, grid, smem)) continue;
-      const int fit = max_clusters(bits, uw, M > 4 ? 2 : 1, p.gpm, ks, smem);
+      const int fit = max_clusters(bits, uw, M > 4 ? 2 : 1, p.gpm, ks, smem, 32 * (p.warp0 + p.nwarps));
       if (fit < 1) continue;
       if (fit < ncl) {
         ncl = fit;
         if (!plan_tc_split(bits, M, N, K, group, ks, ncl, p, uw, grid, smem)) continue;
-        if (max_clusters(bits, uw, M > 4 ? 2 : 1, p.gpm, ks, smem) < ncl) continue;
+        if (max_clusters(bits, uw, M > 4 ? 2 : 1, p.gpm, ks, smem, 32 * (p.warp0 + p.nwarps)) < ncl) continue;
       }
       planned = true;
     }
