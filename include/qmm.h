@@ -245,7 +245,7 @@ int qmm_check(qmm_stream_t stream);
  * qmm_test_timeout_next_decode -- test hook for the failure path above.  The
  *   next decode launch that runs on the tensor-core decode kernel (qmm_gemv
  *   or the argmax heads: INT4 products of more than 2^21 weights or of two
- *   or more tokens, INT8 with 5 to 8 tokens, Q1 with 2 to 8 tokens) has its first
+ *   or more tokens, INT8 with 3 to 8 tokens, Q1 with 2 to 8 tokens) has its first
  *   consumer warp wait on a barrier that is never completed, with a limit of
  *   limit_ns instead of the normal 2 s.  That wait runs out: the launch
  *   writes no output (an argmax head writes idx = 2147483647 and val =

@@ -406,8 +406,8 @@ cudaError_t launch_gemv(const float *x, const uint32_t *codes, const uint16_t *s
     cudaError_t e = launch_gemv_q1(x, codes, scales, y, N, K, group, s);
     if (e != cudaErrorNotSupported) return e;
   }
-  if (M >= 2 && ((bits == 8 && M >= 5) || bits == 1)) {
-    // 8-bit codes with 5 to 8 tokens and binary codes with 2 to 8 tokens: the
+  if (M >= 2 && ((bits == 8 && M >= 3) || bits == 1)) {
+    // 8-bit codes with 3 to 8 tokens and binary codes with 2 to 8 tokens: the
     // tensor-core kernel with K split over a cluster (measured faster)
     cudaError_t e = launch_gemv_tc(x, codes, scales, biases, y, M, N, K, bits, group, s);
     if (e != cudaErrorNotSupported) return e;

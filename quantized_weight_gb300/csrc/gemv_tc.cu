@@ -267,8 +267,8 @@ __host__ __device__ __forceinline__ int run_begin(int w, int W, int total) {
 // cluster.  Separate instantiations keep each kernel's code to the
 // layout it runs (code a kernel carries but never runs measured 2 % slower).
 template <int FMT, int UW, int MT, int GPM, bool ARGMAX, int LAY>
-__global__ void __launch_bounds__(LAY == 1 || (LAY == 2 && MT == 2) ? kThreadsRing : kThreads,
-                                  MT == 1 && LAY != 1 ? 2 : 1)
+__global__ void __launch_bounds__(LAY == 1 || (LAY == 2 && (MT == 2 || FMT == 8)) ? kThreadsRing : kThreads,
+                                  MT == 1 && LAY != 1 && !(LAY == 2 && FMT == 8) ? 2 : 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                    const __grid_constant__ CUtensorMap tm_biases, const TcParams p) {
   using F = Fmt<FMT>;
@@ -1223,17 +1223,18 @@ bool plan_tc_split(int fmt, int M, int64_t N, int64_t K, int group, int ks, int 
   const int spt = npos / uw;
   // each of the S ring slots has nks consumer warps (S * nks <= the
   // consumer warps) taking its tiles in order; nks is chosen for the shortest
-  // longest warp.  Kernels for 5 to 8 tokens may run 16 consumer warps
-  // instead of 15 (a 17th warp) with one or two per slot, taken only where
-  // that shortens the longest warp: measured 25 % faster with 8-bit codes
-  // (a ring slot per tile), and 18 % slower for 4-bit codes with eight warps
-  // per slot (a two-stage ring)
+  // longest warp.  Kernels for 8-bit codes and for 5 to 8 tokens may run 16
+  // consumer warps instead of 15 (a 17th warp) with one or two per slot,
+  // taken only where that shortens the longest warp: measured 25-30 % faster
+  // with 8-bit codes (a ring slot per tile), and 18 % slower for 4-bit codes
+  // with eight warps per slot (a two-stage ring); the Q1 kernels for 2 to 4
+  // tokens keep 16 warps with two CTAs' registers (25 % slower with 17)
   const size_t stage = align1k((size_t)kTileRows * row_bytes + (size_t)ncoef * kTileRows * NG * 2);
   const size_t cl = ((size_t)(ks - 1) * M * rmax * 4 + 4 * (size_t)(ks - 1) + 15) & ~(size_t)15;
   int nks = 0, S = 0, consumers = 15;
   size_t red = 0;
   long best = 0;
-  for (int cons = 15; cons <= (mt == 2 ? 16 : 15); cons++)
+  for (int cons = 15; cons <= (mt == 2 || fmt == 8 ? 16 : 15); cons++)
   for (int c = 1; c <= 8 && c <= spt && spt % c == 0; c <<= 1) {
     if (cons == 16 && c > 2) break;
     const int sc = std::min(nt_w, cons / c);
@@ -1538,9 +1539,9 @@ void plan_store(const PlanKey &k, const PlanVal &v) {
 bool plan_gemv_tc(int M, int64_t N, int64_t K, int bits, int group, TcParams &p, int &uw, int &grid,
                   size_t &smem) {
   bool planned = false;
-  // the K split is measured faster for 8-bit codes with 5 to 8 tokens and
+  // the K split is measured faster for 8-bit codes with 3 to 8 tokens and
   // for binary codes; otherwise it is the fallback of the resident-slab plan
-  const bool split_first = (bits == 8 && M >= 5) || (bits == 1 && M >= 2);
+  const bool split_first = (bits == 8 && M >= 3) || (bits == 1 && M >= 2);
   if (M >= 2 && !split_first) planned = plan_tc(bits, M, N, K, group, false, p, uw, grid, smem);
   if (M >= 2 && !planned) {
     // K split over a cluster, slices of about 1024 k (the smallest split
