@@ -1539,9 +1539,12 @@ void plan_store(const PlanKey &k, const PlanVal &v) {
 bool plan_gemv_tc(int M, int64_t N, int64_t K, int bits, int group, TcParams &p, int &uw, int &grid,
                   size_t &smem) {
   bool planned = false;
-  // the K split is measured faster for 8-bit codes with 3 to 8 tokens and
-  // for binary codes; otherwise it is the fallback of the resident-slab plan
-  const bool split_first = (bits == 8 && M >= 3) || (bits == 1 && M >= 2);
+  // the K split is measured faster for 8-bit codes with 3 to 8 tokens, for
+  // binary codes, and for 4-bit codes with 3 or more tokens over K >= 4096
+  // (whose activation operand leaves the slab one CTA per SM: the down
+  // projection K = 6144 at 4 tokens 8.1 -> 7.5 us; at 2 tokens the slab is
+  // faster); otherwise it is the fallback of the resident-slab plan
+  const bool split_first = (bits == 8 && M >= 3) || (bits == 1 && M >= 2) || (bits == 4 && M >= 3 && K >= 4096);
   if (M >= 2 && !split_first) planned = plan_tc(bits, M, N, K, group, false, p, uw, grid, smem);
   if (M >= 2 && !planned) {
     // K split over a cluster, slices of about 1024 k (the smallest split
