@@ -206,20 +206,24 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float *__restr
                                                              uint16_t *__restrict__ scales,
                                                              uint16_t *__restrict__ biases, int64_t words) {
   const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  // the next word's 32 bytes are loaded before the current word is worked on
+  // (two loads in flight per thread)
+  const float4 *w4 = reinterpret_cast<const float4 *>(w);
+  const float4 nan4 = make_float4(__int_as_float(0x7FC00000), __int_as_float(0x7FC00000),
+                                  __int_as_float(0x7FC00000), __int_as_float(0x7FC00000));
+  int64_t base = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) - lane;
+  float4 na = nan4, nc = nan4;
+  if (base + lane < words) na = w4[2 * (base + lane)], nc = w4[2 * (base + lane) + 1];
   // the loop bound is uniform per warp so that every lane takes part in the shuffles
-  for (int64_t base = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) - lane; base < words;
-       base += (int64_t)gridDim.x * blockDim.x) {
+  for (; base < words; base += stride) {
     const int64_t i = base + lane;
     const bool active = i < words;
+    const float4 a = na, c = nc;
+    if (i + stride < words) na = w4[2 * (i + stride)], nc = w4[2 * (i + stride) + 1];
+    else na = nan4, nc = nan4;
     float v[8];
-    if (active) {
-      const float4 a = reinterpret_cast<const float4 *>(w)[2 * i];
-      const float4 c = reinterpret_cast<const float4 *>(w)[2 * i + 1];
-      v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = c.x, v[5] = c.y, v[6] = c.z, v[7] = c.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; j++) v[j] = __int_as_float(0x7FC00000);
-    }
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = c.x, v[5] = c.y, v[6] = c.z, v[7] = c.w;
     int kmin = 0x7FFFFFFF, kmax = (int)0x80000000;            // no value yet (NaN weights are skipped)
 #pragma unroll
     for (int j = 0; j < 8; j++)
