@@ -49,12 +49,15 @@
 // blocks; the engine's cost is per copy, so a few large copies replace one
 // per row.  The copies do not depend on the previous kernel in the stream,
 // so they are issued before the programmatic-dependent-launch wait.  The 16
-// warps then take runs of (16-row tile, k-step) work.  Longer slabs (a
-// vocabulary head) stream through a ring of 16-row stages fed by a producer
-// warp, and their work units (tile, K slice) go to 15 or 16 consumer warps,
-// each ring slot's own.  Partial sums land in per-(unit, row, token) shared-memory slots;
-// after a barrier one thread per output adds them in a fixed order: no
-// atomics, the same bits on every run.
+// warps then take runs of (16-row tile, k-step) work (for 4-bit codes in
+// groups of 64 with one token, of whole group sets: a lane quad's four
+// groups, two k-steps), the first (units % 16) warps one unit more, so that
+// the four warp schedulers get equal shares.  Longer slabs (a vocabulary
+// head) stream through a ring of 16-row stages fed by a producer warp, and
+// their work units (tile, K slice) go to 15 or 16 consumer warps, each ring
+// slot's own.  Partial sums land in per-(unit, row, token) shared-memory
+// slots; after a barrier one thread per output adds them in a fixed order:
+// no atomics, the same bits on every run.
 //
 // K split over a cluster (two to eight tokens).  The activation operand of
 // eight tokens over the whole K does not fit beside a slab, so these products
@@ -64,7 +67,9 @@
 // the activation operand of its slice only; ranks 1 .. ks-1 write their row
 // totals into rank 0's shared memory (distributed shared memory) and rank 0
 // adds them in rank order after a cluster barrier.  These are separate
-// kernel instantiations, so the one-CTA kernels carry none of it.
+// kernel instantiations, so the one-CTA kernels carry none of it; those for
+// 8-bit codes or five to eight tokens may run a 17th warp (16 consumers),
+// which the plan takes where it gives each tile its own ring slot.
 //
 // Every mbarrier wait is bounded (bounded_wait.cuh); a wait that runs out
 // aborts the CTA, drains its outstanding copies and records
