@@ -173,7 +173,8 @@ BATCH = [(2, 6144, 2048, 4, 64), (4, 6144, 2048, 4, 64), (8, 2048, 6144, 4, 64),
 # slab does not fit (the split is their fallback)
 SPLIT = [(8, 5, 4096, 8, 64), (5, 4000, 8192, 8, 64), (6, 3001, 2048, 8, 128), (7, 2333, 3072, 8, 64),
          (2, 17408, 5120, 1, 128), (3, 4000, 5120, 1, 128), (8, 17408, 5120, 1, 128), (4, 7000, 4096, 1, 128),
-         (2, 3000, 2048, 1, 64), (8, 2048, 6144, 4, 64), (7, 1000, 6144, 4, 64)]
+         (2, 3000, 2048, 1, 64), (8, 2048, 6144, 4, 64), (7, 1000, 6144, 4, 64),
+         (4, 2048, 6144, 4, 64), (3, 1000, 4096, 4, 32), (3, 777, 4096, 8, 64), (4, 2000, 2048, 8, 128)]
 
 
 @pytest.mark.parametrize("M,N,K,bits,group", SPLIT)
